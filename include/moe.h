@@ -1,0 +1,242 @@
+/*
+ * libmoe: a B300 (sm_103a) MoE expert layer behind a plain C ABI.
+ *
+ * The layer is the one described in "Efficient MoE Training for Biological
+ * Foundation Models" (NVIDIA Developer Blog): top-k routing, a permute of the
+ * routed tokens into contiguous per-expert groups, a grouped FC1 GEMM
+ * (gate and up projections, out_features = 2*intermediate_size), SwiGLU
+ * scaled by the routing probabilities ("ScaledSwiGLU"), a grouped FC2
+ * ("down") GEMM and the weighted combine, forward and backward, in BF16 and
+ * in MXFP8 (E4M3 elements, one E8M0 scale per 32 consecutive values).
+ *
+ * Conventions for every call
+ *  - All pointers are DEVICE pointers unless stated otherwise; the caller
+ *    owns every buffer. The library never allocates device memory.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and never synchronise the host, except
+ *    moe_device_error.
+ *  - BF16 tensors are passed as void* and hold IEEE bfloat16 values,
+ *    row-major with the stated leading dimension.
+ *  - Arguments are checked on the host; a bad argument returns MOE_ERR_ARG
+ *    and enqueues nothing. A failed launch returns MOE_ERR_CUDA.
+ *  - Kernels that detect a bad value (an expert index out of range) or give
+ *    up a bounded wait record a flag in a device error word instead of
+ *    trapping; moe_device_error reads and clears it.
+ *
+ * Notation: T tokens, H hidden size, F FFN (intermediate) size, E experts,
+ * k experts per token, R = T*k routed rows, R_pad = rows after padding each
+ * expert group to a multiple of `align`.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef struct CUstream_st* moe_stream_t;
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_ARG = 1,          /* invalid argument; nothing was enqueued */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid but not supported (shape or device) */
+  MOE_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+  MOE_ERR_DEVICE = 4        /* the device error word was set */
+};
+
+/* Device error word flags (moe_device_error). */
+#define MOE_DEVERR_BAD_INDEX 0x1u   /* an expert index outside [0, E) */
+#define MOE_DEVERR_TIMEOUT 0x2u     /* a bounded wait in a pipelined kernel gave up */
+#define MOE_DEVERR_CAPACITY 0x4u    /* more padded rows than the buffer holds */
+#define MOE_DEVERR_LAYOUT 0x8u      /* group offsets not aligned as the call requires */
+
+/* Human-readable name of a status code. Static string; never NULL. */
+MOE_API const char* moe_status_string(int status);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device. *flags (host pointer) receives the MOE_DEVERR_* bits.
+ * Returns MOE_ERR_DEVICE when any bit was set, MOE_OK otherwise. */
+MOE_API int moe_device_error(moe_stream_t stream, unsigned* flags);
+
+/* ------------------------------------------------------------------------
+ * Routing. "How MoE Architecture Cuts Costs and Boosts Efficiency: Efficient
+ * Training of Biological Foundation Models", the Router paragraph (top-K
+ * routing); "Efficient MoE Training ...", §Challenge 1 (routing_weights).
+ *
+ * moe_route: for each token t, the k experts with the largest logits (ties
+ * to the lower expert index; +0 and -0 are equal), in descending order, and
+ * w[t, j] = softmax over those k logits.
+ *   logits  [T, E] fp32, row-major.      idx [T, k] int32 (out).
+ *   w       [T, k] fp32 (out).
+ * Requires 1 <= k <= E <= 256, k <= 8, T >= 0. NaN logits give unspecified
+ * (but in-range) indices.
+ */
+MOE_API int moe_route(const float* logits, int T, int E, int k, int32_t* idx, float* w,
+              moe_stream_t stream);
+
+/* moe_route_backward: gradient of the loss with respect to the logits.
+ * dp holds partial sums of dL/dw: for routed row i = t*k + j the partials are
+ * dp[row(i) * ld_dp + c], c = 0..n_part-1, with row(i) = dest[i] when dest is
+ * not NULL and row(i) = i otherwise. They are summed in increasing c (a fixed
+ * order, so the result is deterministic) into g_j, and
+ *   dlogits[t, e] = w_j * (g_j - sum_i w_i g_i)  if e = idx[t, j],  else 0.
+ *   w, idx [T, k] as produced by moe_route.   dlogits [T, E] fp32 (out).
+ */
+MOE_API int moe_route_backward(const float* dp, long long ld_dp, int n_part, const int32_t* dest,
+                       const float* w, const int32_t* idx, int T, int E, int k,
+                       float* dlogits, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Expert sort: the per-expert token lists and split sizes of
+ * "Efficient MoE Training ...", §Challenge 1, built as a stable counting
+ * sort of the T*k routed rows by expert.
+ *
+ * moe_rows_padded_max: host-side upper bound on R_pad for any routing:
+ *   T*k + E*(align-1). Needs no device access.
+ * moe_permute_plan_workspace_size: bytes of device workspace that
+ *   moe_permute_plan needs (a multiple of 256).
+ *
+ * moe_permute_plan:
+ *   idx      [T, k] int32 expert of each routed row (input).
+ *   counts   [E] int32 (out): rows routed to each expert (the split sizes).
+ *   offsets  [E+1] int32 (out): exclusive prefix sum of counts rounded up to
+ *            `align`; offsets[E] = R_pad. Expert e owns Xp rows
+ *            [offsets[e], offsets[e+1]).
+ *   dest     [T*k] int32 (out): Xp row of routed row i = t*k + j. Inside an
+ *            expert group the rows keep increasing i (token, then slot).
+ *   src      [src_rows] int32 (out): inverse of dest, -1 on padding rows and
+ *            on every row at or beyond R_pad. src_rows must be at least
+ *            moe_rows_padded_max(T, E, k, align).
+ *   workspace, workspace_bytes: device scratch, at least
+ *            moe_permute_plan_workspace_size(T, E, k) bytes, 256-aligned.
+ * Requires 1 <= k <= E <= 1024, 1 <= align <= 4096, T*k < 2^31.
+ * An index outside [0, E) sets MOE_DEVERR_BAD_INDEX and that row is dropped.
+ */
+MOE_API long long moe_rows_padded_max(int T, int E, int k, int align);
+MOE_API size_t moe_permute_plan_workspace_size(int T, int E, int k);
+MOE_API int moe_permute_plan(const int32_t* idx, int T, int E, int k, int align, int32_t* counts,
+                     int32_t* offsets, int32_t* dest, int32_t* src, long long src_rows,
+                     void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* moe_permute: the gather that makes each expert's rows contiguous
+ * ("Efficient MoE Training ...", §Challenge 1, GroupedLinear "gathering ...
+ * input tokens"): xp[dest[t*k + j]] = x[t]; padding rows
+ * [offsets[e] + counts[e], offsets[e+1]) are set to zero.
+ *   x [T, H] bf16.  xp [R_pad, H] bf16 (out).
+ *   w, p_rows: optional (both NULL or both set): p_rows[dest[i]] = w[i]
+ *   (fp32 [R_pad], 0 on padding rows), the per-row routing weight used by
+ *   the scaled-SwiGLU epilogue.
+ * Requires H % 8 == 0 and 16-byte aligned x and xp. */
+MOE_API int moe_permute(const void* x, const int32_t* dest, const int32_t* offsets,
+                const int32_t* counts, const float* w, int T, int H, int E, int k, void* xp,
+                float* p_rows, moe_stream_t stream);
+
+/* moe_unpermute: the combine (index_add of "Efficient MoE Training ...",
+ * §Challenge 1): out[t] = sum_{j<k} w[t, j] * y[dest[t*k + j]], accumulated
+ * in fp32 in slot order j = 0..k-1 and rounded once to bf16. w = NULL means
+ * all weights 1 (used when the weights were already applied, and for the
+ * backward of moe_permute).
+ *   y [R_pad, H] bf16.  out [T, H] bf16 (out).  Requires H % 8 == 0. */
+MOE_API int moe_unpermute(const void* y, const int32_t* dest, const float* w, int T, int H, int k,
+                  void* out, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * MXFP8 quantisation ("Efficient MoE Training ...", §Challenge 2: a scale
+ * for each block of 32 consecutive values; OCP Microscaling Formats v1.0):
+ * per block, e = clamp(floor(log2(max|v|)) - 8, -127, 127) (all-zero block:
+ * -127), scale byte e + 127, element = E4M3(v * 2^-e) rounded to nearest
+ * even and saturated to +-448; a block holding Inf or NaN gets scale 0xFF
+ * and element bytes 0x7F.
+ *
+ * Scale layout (MXFP8 operand with MN rows and K columns, data [MN, K]
+ * e4m3 with K contiguous): 512-byte tiles, one per 128 rows x 128 columns;
+ * tile (i, j) starts at byte (i*(K/128) + j)*512, and inside it the scale of
+ * row r = 32a + b (b < 32, a < 4) and 32-column block c (c < 4) is byte
+ * 16b + 4a + c. This is the order in which tcgen05 block-scaled MMAs take
+ * scales from tensor memory.
+ *
+ * mxfp8_quantize: input rows r = 0..rows-1 are read from in + row(r)*ld,
+ * with row(r) = r when src is NULL, else row(r) = src[r] / src_div, and a
+ * zero row when src[r] < 0 (this fuses moe_permute into the quantiser).
+ *   dirs & 1 (row-wise, blocks along a row):  q_row [rows, cols] e4m3,
+ *       s_row tiled with MN = rows, K = cols.
+ *   dirs & 2 (column-wise, blocks of 32 rows, stored transposed):
+ *       q_col [cols, rows] e4m3, s_col tiled with MN = cols, K = rows.
+ * Requires rows % 128 == 0, cols % 128 == 0, ld >= cols, ld % 8 == 0. */
+#define MOE_QUANT_ROWWISE 1
+#define MOE_QUANT_COLWISE 2
+MOE_API int mxfp8_quantize(const void* in, long long rows, int cols, long long ld, const int32_t* src,
+                   int src_div, int dirs, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                   uint8_t* s_col, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Grouped GEMM on tcgen05 tensor cores: one launch for all experts, each with
+ * its own weights and its own number of rows ("Efficient MoE Training ...",
+ * §Challenge 1: GroupedLinear takes per-expert token counts, split_sizes, and
+ * submits all local experts as one grouped operation).
+ *
+ * Groups: expert e owns rows [offsets[e], offsets[e+1]) of the row-indexed
+ * operands; offsets is the device array written by moe_permute_plan.
+ *
+ * moe_grouped_gemm_bf16, mode MOE_GEMM_FPROP (forward and dgrad):
+ *   C[r, n] = sum_k A[r, k] * B_e(k, n) for every row r of group e.
+ *   A [rows, K] bf16, C [rows, N] bf16 (fp32 accumulation, one rounding).
+ *   b_layout 0: B_e stored [K, N] at B + e*K*N (N contiguous).
+ *   b_layout 1: B_e stored [N, K] at B + e*N*K (K contiguous), i.e. B_e^T.
+ *   M is ignored. Requires N % 128 == 0, K % 64 == 0.
+ * mode MOE_GEMM_WGRAD (weight gradients):
+ *   C_e[m, n] = sum over rows r of group e of A[r, m] * B[r, n];
+ *   C_e = C + e*M*N, [M, N] bf16. A [rows, M], B [rows, N] bf16.
+ *   Experts with no rows get C_e = 0. Requires M % 128 == 0, N % 128 == 0,
+ *   and every group size a multiple of 64 (else MOE_DEVERR_LAYOUT).
+ * All of A, B, C 16-byte aligned; 1 <= E <= 256; rows < 2^31.
+ */
+#define MOE_GEMM_FPROP 0
+#define MOE_GEMM_WGRAD 1
+MOE_API int moe_grouped_gemm_bf16(int mode, const void* A, const void* B, int b_layout,
+                                  const int32_t* offsets, int E, long long rows, int M, int N,
+                                  int K, void* C, moe_stream_t stream);
+
+/* moe_fc1_swiglu_bf16: the fused gate_up GroupedLinear + ScaledSwiGLU of
+ * "Efficient MoE Training ...", §Challenge 3. For every row r of group e:
+ *   [g | u] = xp[r] * W1_e  (W1_e stored [H, 2F], gate = columns [0, F)),
+ *   gu[r] = [g | u] rounded to bf16 (kept for the backward),
+ *   h[r, f] = silu(g_f) * u_f * p_rows[r]  (bf16), silu(z) = z / (1 + e^-z).
+ *   xp [rows, H], w1 [E, H, 2F], gu [rows, 2F], h [rows, F] bf16;
+ *   p_rows [rows] fp32 (moe_permute's per-row routing weight).
+ * Requires H % 64 == 0, F % 64 == 0. */
+MOE_API int moe_fc1_swiglu_bf16(const void* xp, const void* w1, const int32_t* offsets,
+                                const float* p_rows, int E, long long rows, int H, int F,
+                                void* gu, void* h, moe_stream_t stream);
+
+/* moe_swiglu_bwd_parts: number of partial sums per row that
+ * moe_fc2_dgrad_swiglu_bwd_bf16 writes to dp_part (0 if F is unsupported). */
+MOE_API int moe_swiglu_bwd_parts(int F);
+
+/* moe_fc2_dgrad_swiglu_bwd_bf16: the matching fused backward. For every row
+ * r of group e: dH = dy2[r] * W2_e^T (W2_e stored [F, H]); with g, u from gu
+ * and p = p_rows[r]: a = silu(g)*u, dA = dH*p,
+ *   dy1[r] = [dA*u*silu'(g) | dA*silu(g)]  (bf16, [rows, 2F]),
+ *   dp_part[r, c] = sum over the c-th block of F columns of dH*a (fp32),
+ *   c < moe_swiglu_bwd_parts(F); sum them with moe_route_backward.
+ * silu'(z) = s(z)*(1 + z*(1 - s(z))), s the logistic function.
+ * Requires H % 64 == 0, F % 128 == 0. */
+MOE_API int moe_fc2_dgrad_swiglu_bwd_bf16(const void* dy2, const void* w2,
+                                          const int32_t* offsets, const float* p_rows,
+                                          const void* gu, int E, long long rows, int H, int F,
+                                          void* dy1, float* dp_part, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

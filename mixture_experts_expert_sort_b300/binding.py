@@ -1,0 +1,240 @@
+"""Thin ctypes binding of libmoe (include/moe.h): argument marshalling only.
+
+Every function here takes torch CUDA tensors, checks nothing beyond what
+ctypes needs, passes raw device pointers and the current CUDA stream to the C
+entry point of the same name, and raises on a non-zero status. All
+computation happens in the library's kernels; if the library is missing this
+module raises instead of computing anything elsewhere.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+_lib = None
+
+MOE_OK, MOE_ERR_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(5)
+MOE_DEVERR_BAD_INDEX, MOE_DEVERR_TIMEOUT, MOE_DEVERR_CAPACITY = 1, 2, 4
+QUANT_ROWWISE, QUANT_COLWISE = 1, 2
+GEMM_FPROP, GEMM_WGRAD = 0, 1
+
+_p, _i, _ll, _sz, _u = C.c_void_p, C.c_int, C.c_longlong, C.c_size_t, C.c_uint
+
+# name -> (restype, argtypes); mirrors include/moe.h
+SIGNATURES = {
+    "moe_status_string": (C.c_char_p, [_i]),
+    "moe_device_error": (_i, [_p, C.POINTER(_u)]),
+    "moe_route": (_i, [_p, _i, _i, _i, _p, _p, _p]),
+    "moe_route_backward": (_i, [_p, _ll, _i, _p, _p, _p, _i, _i, _i, _p, _p]),
+    "moe_rows_padded_max": (_ll, [_i, _i, _i, _i]),
+    "moe_permute_plan_workspace_size": (_sz, [_i, _i, _i]),
+    "moe_permute_plan": (_i, [_p, _i, _i, _i, _i, _p, _p, _p, _p, _ll, _p, _sz, _p]),
+    "moe_permute": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _p, _p, _p]),
+    "moe_unpermute": (_i, [_p, _p, _p, _i, _i, _i, _p, _p]),
+    "mxfp8_quantize": (_i, [_p, _ll, _i, _ll, _p, _i, _i, _p, _p, _p, _p, _p]),
+    "moe_grouped_gemm_bf16": (_i, [_i, _p, _p, _i, _p, _i, _ll, _i, _i, _i, _p, _p]),
+    "moe_fc1_swiglu_bf16": (_i, [_p, _p, _p, _p, _i, _ll, _i, _i, _p, _p, _p]),
+    "moe_swiglu_bwd_parts": (_i, [_i]),
+    "moe_fc2_dgrad_swiglu_bwd_bf16": (_i, [_p, _p, _p, _p, _p, _i, _ll, _i, _i, _p, _p, _p]),
+}
+
+
+class MoeError(RuntimeError):
+    pass
+
+
+def lib():
+    """Load libmoe.so (built in-tree by mixture_experts_expert_sort_b300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise MoeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m mixture_experts_expert_sort_b300.build`")
+        L = C.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != MOE_OK:
+        msg = lib().moe_status_string(status).decode()
+        raise MoeError(f"{what} failed: {msg}")
+
+
+def ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def stream_handle(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def device_error(stream=None) -> int:
+    flags = C.c_uint(0)
+    st = lib().moe_device_error(stream_handle(stream), C.byref(flags))
+    if st not in (MOE_OK, MOE_ERR_DEVICE):
+        _check(st, "moe_device_error")
+    return flags.value
+
+
+# ----------------------------------------------------------------- routing
+
+def moe_route(logits, k, idx=None, w=None, stream=None):
+    T, E = logits.shape
+    dev = logits.device
+    idx = idx if idx is not None else torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = w if w is not None else torch.empty((T, k), dtype=torch.float32, device=dev)
+    _check(lib().moe_route(ptr(logits), T, E, k, ptr(idx), ptr(w), stream_handle(stream)),
+           "moe_route")
+    return idx, w
+
+
+def moe_route_backward(dp, w, idx, E, dest=None, dlogits=None, stream=None):
+    """dp: [rows, n_part] fp32 partials (rows indexed by dest if given, else flat t*k+j)."""
+    T, k = idx.shape
+    dp2 = dp if dp.dim() == 2 else dp.reshape(-1, 1)
+    dlogits = dlogits if dlogits is not None else torch.empty((T, E), dtype=torch.float32,
+                                                              device=idx.device)
+    _check(lib().moe_route_backward(ptr(dp2), dp2.stride(0), dp2.shape[1], ptr(dest), ptr(w),
+                                    ptr(idx), T, E, k, ptr(dlogits), stream_handle(stream)),
+           "moe_route_backward")
+    return dlogits
+
+
+# ------------------------------------------------------------ expert sort
+
+def moe_rows_padded_max(T, E, k, align):
+    return int(lib().moe_rows_padded_max(T, E, k, align))
+
+
+def moe_permute_plan_workspace_size(T, E, k):
+    return int(lib().moe_permute_plan_workspace_size(T, E, k))
+
+
+def moe_permute_plan(idx, E, align, src_rows=None, workspace=None, stream=None, out=None):
+    T, k = idx.shape
+    dev = idx.device
+    rmax = moe_rows_padded_max(T, E, k, align)
+    src_rows = rmax if src_rows is None else src_rows
+    if out is None:
+        out = {
+            "counts": torch.empty(E, dtype=torch.int32, device=dev),
+            "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+            "dest": torch.empty(max(T * k, 1), dtype=torch.int32, device=dev),
+            "src": torch.empty(max(src_rows, 1), dtype=torch.int32, device=dev),
+        }
+    wsb = moe_permute_plan_workspace_size(T, E, k)
+    if workspace is None:
+        workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    _check(lib().moe_permute_plan(ptr(idx), T, E, k, align, ptr(out["counts"]),
+                                  ptr(out["offsets"]), ptr(out["dest"]), ptr(out["src"]),
+                                  src_rows, ptr(workspace), workspace.numel(),
+                                  stream_handle(stream)), "moe_permute_plan")
+    return out
+
+
+def moe_permute(x, dest, offsets, counts, k, rows, w=None, xp=None, p_rows=None, stream=None):
+    T, H = x.shape
+    E = counts.numel()
+    dev = x.device
+    xp = xp if xp is not None else torch.empty((rows, H), dtype=x.dtype, device=dev)
+    if w is not None and p_rows is None:
+        p_rows = torch.empty(rows, dtype=torch.float32, device=dev)
+    _check(lib().moe_permute(ptr(x), ptr(dest), ptr(offsets), ptr(counts), ptr(w), T, H, E, k,
+                             ptr(xp), ptr(p_rows), stream_handle(stream)), "moe_permute")
+    return xp, p_rows
+
+
+def moe_unpermute(y, dest, T, k, w=None, out=None, stream=None):
+    H = y.shape[1]
+    out = out if out is not None else torch.empty((T, H), dtype=y.dtype, device=y.device)
+    _check(lib().moe_unpermute(ptr(y), ptr(dest), ptr(w), T, H, k, ptr(out),
+                               stream_handle(stream)), "moe_unpermute")
+    return out
+
+
+# ------------------------------------------------------------------ MXFP8
+
+def mx_scale_bytes(mn, kdim):
+    return (mn // 128) * (kdim // 128) * 512
+
+
+def mxfp8_quantize(x, dirs=QUANT_ROWWISE | QUANT_COLWISE, rows=None, src=None, src_div=1,
+                   stream=None, out=None):
+    """x: [n, cols] bf16 (row stride x.stride(0)). Returns dict of q_row/s_row/q_col/s_col."""
+    cols = x.shape[1]
+    rows = x.shape[0] if rows is None else rows
+    dev = x.device
+    if out is None:
+        out = {}
+        if dirs & QUANT_ROWWISE:
+            out["q_row"] = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+            out["s_row"] = torch.empty(mx_scale_bytes(rows, cols), dtype=torch.uint8, device=dev)
+        if dirs & QUANT_COLWISE:
+            out["q_col"] = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+            out["s_col"] = torch.empty(mx_scale_bytes(cols, rows), dtype=torch.uint8, device=dev)
+    _check(lib().mxfp8_quantize(ptr(x), rows, cols, x.stride(0), ptr(src), src_div, dirs,
+                                ptr(out.get("q_row")), ptr(out.get("s_row")),
+                                ptr(out.get("q_col")), ptr(out.get("s_col")),
+                                stream_handle(stream)), "mxfp8_quantize")
+    return out
+
+
+# ----------------------------------------------------------- grouped GEMM
+
+def moe_grouped_gemm_bf16(mode, A, B, offsets, b_layout=0, M=0, N=0, K=0, C=None, stream=None):
+    """FPROP: C[rows, N] = A[rows] @ B_e per group (B [E,K,N] or [E,N,K]).
+    WGRAD: C[E, M, N] = A_e^T @ B_e over each group's rows (A [rows, M], B [rows, N])."""
+    E = offsets.numel() - 1
+    rows = A.shape[0]
+    if mode == GEMM_FPROP:
+        K = A.shape[1]
+        N = B.shape[2] if b_layout == 0 else B.shape[1]
+        C = C if C is not None else torch.empty((rows, N), dtype=torch.bfloat16, device=A.device)
+    else:
+        M, N = A.shape[1], B.shape[1]
+        C = C if C is not None else torch.empty((E, M, N), dtype=torch.bfloat16, device=A.device)
+    _check(lib().moe_grouped_gemm_bf16(mode, ptr(A), ptr(B), b_layout, ptr(offsets), E, rows, M,
+                                       N, K, ptr(C), stream_handle(stream)),
+           "moe_grouped_gemm_bf16")
+    return C
+
+
+def moe_fc1_swiglu_bf16(xp, w1, offsets, p_rows, gu=None, h=None, stream=None):
+    rows, H = xp.shape
+    E, _, F2 = w1.shape
+    F = F2 // 2
+    gu = gu if gu is not None else torch.empty((rows, F2), dtype=torch.bfloat16, device=xp.device)
+    h = h if h is not None else torch.empty((rows, F), dtype=torch.bfloat16, device=xp.device)
+    _check(lib().moe_fc1_swiglu_bf16(ptr(xp), ptr(w1), ptr(offsets), ptr(p_rows), E, rows, H, F,
+                                     ptr(gu), ptr(h), stream_handle(stream)),
+           "moe_fc1_swiglu_bf16")
+    return gu, h
+
+
+def moe_swiglu_bwd_parts(F):
+    return int(lib().moe_swiglu_bwd_parts(F))
+
+
+def moe_fc2_dgrad_swiglu_bwd_bf16(dy2, w2, offsets, p_rows, gu, dy1=None, dp_part=None,
+                                  stream=None):
+    rows, H = dy2.shape
+    E, F, _ = w2.shape
+    dev = dy2.device
+    dy1 = dy1 if dy1 is not None else torch.empty((rows, 2 * F), dtype=torch.bfloat16, device=dev)
+    if dp_part is None:
+        dp_part = torch.empty((rows, moe_swiglu_bwd_parts(F)), dtype=torch.float32, device=dev)
+    _check(lib().moe_fc2_dgrad_swiglu_bwd_bf16(ptr(dy2), ptr(w2), ptr(offsets), ptr(p_rows),
+                                               ptr(gu), E, rows, H, F, ptr(dy1), ptr(dp_part),
+                                               stream_handle(stream)),
+           "moe_fc2_dgrad_swiglu_bwd_bf16")
+    return dy1, dp_part

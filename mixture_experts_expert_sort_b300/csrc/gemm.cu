@@ -1,0 +1,679 @@
+// Persistent grouped GEMM on the 5th-generation tensor cores (tcgen05), fed
+// by TMA, with fused epilogues.
+//
+// "Efficient MoE Training for Biological Foundation Models", §Challenge 1
+// (GroupedLinear: one grouped operation over all local experts, each with
+// its own weights and its own number of tokens, the split sizes) and
+// §Challenge 3 (the GroupedLinear -> ScaledSwiGLU -> GroupedLinear sequence
+// fused, with the SwiGLU and the routing-probability scaling applied to the
+// FC1 result before it is written, plus a matching fused backward).
+//
+// Structure of one CTA (one per SM, persistent over output tiles):
+//   warp 0      TMA producer: stages A and B tiles (128B swizzle) into a ring
+//               of shared-memory stages, signalling `full` mbarriers.
+//   warp 1      allocates TMEM; one elected thread issues tcgen05.mma for
+//               each stage and commits to the stage's `empty` mbarrier, and
+//               to the accumulator's `tfull` mbarrier at the end of a tile.
+//   warps 2..5  epilogue: tcgen05.ld the fp32 accumulator (each warp owns a
+//               32-lane quarter of TMEM = 32 rows of the tile), apply the
+//               epilogue, store to global memory, release the accumulator.
+// Two accumulators of BN fp32 columns each let the epilogue of one tile run
+// under the main loop of the next.
+//
+// Tiles are 128 x BN x 64 (BF16). Expert groups are visited in order; within
+// a group the m-tiles of one n-tile are adjacent, so a weight tile is read
+// from HBM once and the group's activations stay in L2.
+//
+// Two problem shapes ("modes"):
+//   FPROP: rows [o_e, o_{e+1}) of A times expert e's B (forward and dgrad).
+//   WGRAD: C_e = A_e^T * B_e with the reduction over expert e's rows.
+// Every wait is bounded: after kWaitLimitNs the kernel records
+// MOE_DEVERR_TIMEOUT, stops issuing work, lets its copies land, frees TMEM
+// and returns.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace gemm {
+
+enum Mode { FPROP = 0, WGRAD = 1 };
+enum Epi { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2 };
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // BF16: 64 elements = 128 bytes = one swizzle row
+constexpr int kThreads = 192;
+constexpr int kMaxGroups = 256;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+struct Params {
+  const int32_t* offsets;  // [E+1] group row offsets
+  int E;
+  int M, N, K;  // FPROP: N, K fixed (M per group); WGRAD: M, N fixed (K per group)
+  int F;        // SwiGLU epilogues: FFN width (gate | up split of FC1 columns)
+  int b_kmajor; // FPROP: 1 if expert B is stored [N, K], 0 if [K, N]
+  __nv_bfloat16* C;          // EPI_STORE output, EPI_SWIGLU_BWD dY1 [rows, 2F]
+  long long ldc;
+  long long c_group_stride;  // WGRAD: elements between experts' outputs
+  const float* p_rows;       // per-row routing weight (SwiGLU epilogues)
+  __nv_bfloat16* GU;         // FWD: out [rows, 2F] (gate | up); BWD: in
+  __nv_bfloat16* Hout;       // FWD: out [rows, F]
+  float* dp_part;            // BWD: [rows, n_part] partial dL/dp per n-tile
+  int n_part;
+};
+
+template <int BN>
+struct Smem {
+  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (BN == 256) ? 4 : 6;
+  static constexpr int kBarOffset = kStages * kStageBytes;
+  // full[S], empty[S], tfull[2], tempty[2], drain
+  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
+  // misc: tmem base (4), abort flag (4), tile prefix [kMaxGroups + 1] ints
+  static constexpr int kPrefixOffset = kMiscOffset + 16;
+  static constexpr int kBytes = kPrefixOffset + (kMaxGroups + 1) * 4;
+  static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
+};
+
+struct TileInfo {
+  int e, mt, nt;
+  long long row0;  // FPROP: first row of the group; WGRAD: first reduction row
+  int rows;        // rows in the group
+  int k_iters;
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      raise_device_error(MOE_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Wait for in-flight asynchronous work at kernel exit: bounded by time only.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      raise_device_error(MOE_DEVERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+template <int MODE, int BN>
+__device__ __forceinline__ void decode_tile(const Params& p, const int* prefix, int t, int& e_hint,
+                                            TileInfo& ti) {
+  int e = e_hint;
+  while (prefix[e + 1] <= t) ++e;
+  e_hint = e;
+  const int local = t - prefix[e];
+  const long long o0 = p.offsets[e], o1 = p.offsets[e + 1];
+  ti.e = e;
+  ti.row0 = o0;
+  ti.rows = (int)(o1 - o0);
+  if (MODE == FPROP) {
+    const int mtiles = (ti.rows + BM - 1) / BM;
+    ti.mt = local % mtiles;
+    ti.nt = local / mtiles;
+    ti.k_iters = p.K / BK;
+  } else {
+    const int mtiles = p.M / BM;
+    ti.mt = local % mtiles;
+    ti.nt = local / mtiles;
+    ti.k_iters = ti.rows / BK;
+  }
+}
+
+// Global column of B-tile half h (each half is BN/2 columns wide).
+template <int EPI, int BN>
+__device__ __forceinline__ int b_half_col(const Params& p, int nt, int h) {
+  if (EPI == EPI_SWIGLU_FWD) return h * p.F + nt * (BN / 2);
+  return nt * BN + h * (BN / 2);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float* v) {
+  uint4* o = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    o[q] = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                      pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+}
+
+__device__ __forceinline__ void load32_bf16(const __nv_bfloat16* src, float* v) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u = s[q];
+    v[8 * q + 0] = bf16_lo(u.x);
+    v[8 * q + 1] = bf16_hi(u.x);
+    v[8 * q + 2] = bf16_lo(u.y);
+    v[8 * q + 3] = bf16_hi(u.y);
+    v[8 * q + 4] = bf16_lo(u.z);
+    v[8 * q + 5] = bf16_hi(u.z);
+    v[8 * q + 6] = bf16_lo(u.w);
+    v[8 * q + 7] = bf16_hi(u.w);
+  }
+}
+
+__device__ __forceinline__ float sigmoidf_fast(float z) { return 1.f / (1.f + __expf(-z)); }
+
+template <int MODE, int EPI, int BN, int A_MN, int B_MN>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB, const Params p) {
+  using L = Smem<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const uint32_t bar0 = sbase + L::kBarOffset;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (L::kStages + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * L::kStages + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * L::kStages + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * L::kStages + 4);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::kMiscOffset);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::kMiscOffset + 4);
+  int* s_prefix = reinterpret_cast<int*>(smem + L::kPrefixOffset);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tiles = p.N / BN;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < L::kStages; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(tfull_bar(b), 1);
+      ptx::mbar_init(tempty_bar(b), 128);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    ptx::fence_mbar_init();
+    *s_abort = 0;
+    // Tile prefix over groups.
+    int acc = 0;
+    bool bad = false;
+    s_prefix[0] = 0;
+    for (int e = 0; e < p.E; ++e) {
+      int rows = p.offsets[e + 1] - p.offsets[e];
+      int mt;
+      if (MODE == FPROP) {
+        mt = (rows + BM - 1) / BM;
+      } else {
+        mt = p.M / BM;
+        if (rows % BK) bad = true;
+      }
+      acc += mt * n_tiles;
+      s_prefix[e + 1] = acc;
+    }
+    if (bad) raise_device_error(MOE_DEVERR_LAYOUT);
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(s_tmem), 2 * BN);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int total_tiles = s_prefix[p.E];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (ptx::elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed_phase[L::kStages];
+      bool armed[L::kStages];
+      for (int s = 0; s < L::kStages; ++s) armed[s] = false;
+      int e_hint = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        TileInfo ti;
+        decode_tile<MODE, BN>(p, s_prefix, t, e_hint, ti);
+        for (int kb = 0; kb < ti.k_iters; ++kb) {
+          if (!wait_bar(empty_bar(stage), phase ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t a_dst = sbase + stage * L::kStageBytes;
+          const uint32_t b_dst = a_dst + L::kABytes;
+          ptx::mbar_arrive_expect_tx(full_bar(stage), L::kStageBytes);
+          armed[stage] = true;
+          armed_phase[stage] = phase;
+          const int k0 = kb * BK;
+          if (MODE == FPROP) {
+            // A: rows of the group, K-major, one box of 128 rows x 64 K.
+            ptx::tma_load_2d(a_dst, &tmA, k0, (int)(ti.row0 + (long long)ti.mt * BM),
+                             full_bar(stage));
+            if (B_MN) {
+              // B_e stored [K, N]: BN/64 chunks of [64 K rows][64 N].
+#pragma unroll
+              for (int c = 0; c < BN / 64; ++c) {
+                const int h = c / (BN / 128), off = (c % (BN / 128)) * 64;
+                const int n = b_half_col<EPI, BN>(p, ti.nt, h) + off;
+                ptx::tma_load_2d(b_dst + c * (BK * 128), &tmB, n, ti.e * p.K + k0,
+                                 full_bar(stage));
+              }
+            } else {
+              // B_e stored [N, K]: two boxes of BN/2 rows x 64 K.
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int n = b_half_col<EPI, BN>(p, ti.nt, h);
+                ptx::tma_load_2d(b_dst + h * (BN / 2) * 128, &tmB, k0, ti.e * p.N + n,
+                                 full_bar(stage));
+              }
+            }
+          } else {
+            // WGRAD: A = X [rows, M] and B = Y [rows, N], both MN-major.
+            const int r = (int)(ti.row0 + k0);
+#pragma unroll
+            for (int c = 0; c < BM / 64; ++c)
+              ptx::tma_load_2d(a_dst + c * (BK * 128), &tmA, ti.mt * BM + c * 64, r,
+                               full_bar(stage));
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+              ptx::tma_load_2d(b_dst + c * (BK * 128), &tmB, ti.nt * BN + c * 64, r,
+                               full_bar(stage));
+          }
+          if (++stage == L::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Let every armed copy land before the CTA can exit (bounded).
+      for (int s = 0; s < L::kStages; ++s)
+        if (armed[s]) drain_wait(full_bar(s), armed_phase[s]);
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (ptx::elect_one()) {
+      constexpr uint32_t idesc = ptx::idesc_bf16(BM, BN, MODE == WGRAD ? 1 : A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      int e_hint = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        TileInfo ti;
+        decode_tile<MODE, BN>(p, s_prefix, t, e_hint, ti);
+        if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, s_abort)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < ti.k_iters; ++kb) {
+          if (!wait_bar(full_bar(stage), phase, s_abort)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = sbase + stage * L::kStageBytes;
+          const uint32_t b_addr = a_addr + L::kABytes;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            uint64_t da, db;
+            if (MODE == WGRAD || A_MN)
+              da = ptx::smem_desc(a_addr + kk * 2048, BK * 128, 1024, ptx::kSwizzle128B);
+            else
+              da = ptx::smem_desc(a_addr + kk * 32, 16, 1024, ptx::kSwizzle128B);
+            if (B_MN)
+              db = ptx::smem_desc(b_addr + kk * 2048, BK * 128, 1024, ptx::kSwizzle128B);
+            else
+              db = ptx::smem_desc(b_addr + kk * 32, 16, 1024, ptx::kSwizzle128B);
+            ptx::mma_bf16(d_tmem, da, db, idesc, (kb | kk) ? 1u : 0u);
+          }
+          ptx::mma_commit(empty_bar(stage));
+          if (++stage == L::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (ti.k_iters > 0)
+          ptx::mma_commit(tfull_bar(acc));
+        else
+          ptx::mbar_arrive(tfull_bar(acc));
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // All MMAs issued by this thread complete before TMEM is released.
+      ptx::mma_commit(drain_bar);
+      drain_wait(drain_bar, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;  // row of the tile
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int e_hint = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      TileInfo ti;
+      decode_tile<MODE, BN>(p, s_prefix, t, e_hint, ti);
+      if (!wait_bar(tfull_bar(acc), acc_phase, s_abort)) break;
+      ptx::tc_fence_after();
+      const uint32_t tm = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      const bool has_acc = ti.k_iters > 0;
+      if (MODE == WGRAD) {
+        __nv_bfloat16* crow = p.C + (long long)ti.e * p.c_group_stride +
+                              (long long)(ti.mt * BM + r) * p.ldc + (long long)ti.nt * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          float f[32];
+          if (has_acc) {
+            ptx::tmem_ld_32x32b_x32(tm + c * 32, v);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = 0.f;
+          }
+          store32_bf16(crow + c * 32, f);
+        }
+      } else {
+        const int lrow = ti.mt * BM + r;
+        const bool row_ok = lrow < ti.rows;
+        const long long grow = ti.row0 + lrow;
+        if (EPI == EPI_STORE) {
+          __nv_bfloat16* crow = p.C + grow * p.ldc + (long long)ti.nt * BN;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            float f[32];
+            ptx::tmem_ld_32x32b_x32(tm + c * 32, v);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+            if (row_ok) store32_bf16(crow + c * 32, f);
+          }
+        } else if (EPI == EPI_SWIGLU_FWD) {
+          const float pr = row_ok ? p.p_rows[grow] : 0.f;
+          const int n0 = ti.nt * (BN / 2);
+          const long long F = p.F;
+#pragma unroll 1
+          for (int c = 0; c < BN / 64; ++c) {
+            uint32_t vg[32], vu[32];
+            ptx::tmem_ld_32x32b_x32(tm + c * 32, vg);
+            ptx::tmem_ld_32x32b_x32(tm + BN / 2 + c * 32, vu);
+            ptx::tmem_ld_wait();
+            float g[32], u[32], h[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              g[i] = __uint_as_float(vg[i]);
+              u[i] = __uint_as_float(vu[i]);
+              h[i] = g[i] * sigmoidf_fast(g[i]) * u[i] * pr;
+            }
+            if (row_ok) {
+              const long long col = n0 + c * 32;
+              store32_bf16(p.GU + grow * 2 * F + col, g);
+              store32_bf16(p.GU + grow * 2 * F + F + col, u);
+              store32_bf16(p.Hout + grow * F + col, h);
+            }
+          }
+        } else {  // EPI_SWIGLU_BWD: accumulator holds dH for F-columns [nt*BN, +BN)
+          const float pr = row_ok ? p.p_rows[grow] : 0.f;
+          const int n0 = ti.nt * BN;
+          const long long F = p.F;
+          float dp = 0.f;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(tm + c * 32, v);
+            ptx::tmem_ld_wait();
+            if (row_ok) {
+              const long long col = n0 + c * 32;
+              float g[32], u[32], dg[32], du[32];
+              load32_bf16(p.GU + grow * 2 * F + col, g);
+              load32_bf16(p.GU + grow * 2 * F + F + col, u);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const float dh = __uint_as_float(v[i]);
+                const float s = sigmoidf_fast(g[i]);
+                const float silu = g[i] * s;
+                dp = fmaf(dh, silu * u[i], dp);
+                const float da = dh * pr;
+                dg[i] = da * u[i] * s * (1.f + g[i] * (1.f - s));
+                du[i] = da * silu;
+              }
+              store32_bf16(p.C + grow * p.ldc + col, dg);
+              store32_bf16(p.C + grow * p.ldc + F + col, du);
+            }
+          }
+          if (row_ok) p.dp_part[grow * p.n_part + ti.nt] = dp;
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(tempty_bar(acc));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, 2 * BN);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2-D row-major tensor [rows, cols] of `elem_bytes` elements, box [box_rows, box_cols],
+// 128-byte swizzle (box_cols * elem_bytes must be <= 128).
+static bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes,
+                      long long rows, long long cols, long long ld, int box_rows, int box_cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * elem_bytes)};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+template <int MODE, int EPI, int BN, int A_MN, int B_MN>
+static int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
+                  long long tiles_bound, cudaStream_t st) {
+  auto kern = grouped_gemm_bf16_kernel<MODE, EPI, BN, A_MN, B_MN>;
+  const int smem = Smem<BN>::kAlloc;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set = true;
+  }
+  long long grid = tiles_bound < num_sms() ? tiles_bound : num_sms();
+  if (grid < 1) grid = 1;
+  kern<<<(unsigned)grid, kThreads, smem, st>>>(ta, tb, p);
+  return launch_status();
+}
+
+}  // namespace gemm
+}  // namespace moe
+
+using namespace moe;
+using namespace moe::gemm;
+
+namespace {
+constexpr CUtensorMapDataType kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+
+bool gemm_common_ok(const void* A, const void* B, const void* C, const int32_t* offsets, int E) {
+  return A && B && C && offsets && E >= 1 && E <= kMaxGroups && aligned16(A) && aligned16(B) &&
+         aligned16(C);
+}
+}  // namespace
+
+extern "C" int moe_grouped_gemm_bf16(int mode, const void* A, const void* B, int b_layout,
+                                     const int32_t* offsets, int E, long long rows, int M, int N,
+                                     int K, void* C, moe_stream_t stream) {
+  if (!gemm_common_ok(A, B, C, offsets, E) || rows < 0 || rows >= (1LL << 31)) return MOE_ERR_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  Params p{};
+  p.offsets = offsets;
+  p.E = E;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.C = static_cast<__nv_bfloat16*>(C);
+  CUtensorMap ta, tb;
+  if (mode == MOE_GEMM_FPROP) {
+    if (N < 128 || N % 128 || K < BK || K % BK || (b_layout != 0 && b_layout != 1))
+      return MOE_ERR_ARG;
+    if (rows == 0) return MOE_OK;
+    p.ldc = N;
+    p.b_kmajor = b_layout;
+    const bool bn256 = (N % 256) == 0;
+    if (!make_tmap(&ta, A, kBF16, 2, rows, K, K, BM, BK)) return MOE_ERR_CUDA;
+    if (b_layout == 0) {
+      if (!make_tmap(&tb, B, kBF16, 2, (long long)E * K, N, N, BK, 64)) return MOE_ERR_CUDA;
+    } else {
+      if (!make_tmap(&tb, B, kBF16, 2, (long long)E * N, K, K, bn256 ? 128 : 64, BK))
+        return MOE_ERR_CUDA;
+    }
+    long long bound = (rows / BM + E) * (long long)(N / 128);
+    if (bn256)
+      return b_layout ? launch<FPROP, EPI_STORE, 256, 0, 0>(ta, tb, p, bound, st)
+                      : launch<FPROP, EPI_STORE, 256, 0, 1>(ta, tb, p, bound, st);
+    return b_layout ? launch<FPROP, EPI_STORE, 128, 0, 0>(ta, tb, p, bound, st)
+                    : launch<FPROP, EPI_STORE, 128, 0, 1>(ta, tb, p, bound, st);
+  }
+  if (mode == MOE_GEMM_WGRAD) {
+    if (M < BM || M % BM || N < 128 || N % 128) return MOE_ERR_ARG;
+    p.ldc = N;
+    p.c_group_stride = (long long)M * N;
+    const bool bn256 = (N % 256) == 0;
+    if (rows > 0) {
+      if (!make_tmap(&ta, A, kBF16, 2, rows, M, M, BK, 64)) return MOE_ERR_CUDA;
+      if (!make_tmap(&tb, B, kBF16, 2, rows, N, N, BK, 64)) return MOE_ERR_CUDA;
+    } else {
+      // No rows at all: every expert's gradient is zero; maps are never read.
+      if (!make_tmap(&ta, C, kBF16, 2, M, N, N, BK, 64)) return MOE_ERR_CUDA;
+      tb = ta;
+    }
+    long long bound = (long long)E * (M / BM) * (N / 128);
+    return bn256 ? launch<WGRAD, EPI_STORE, 256, 1, 1>(ta, tb, p, bound, st)
+                 : launch<WGRAD, EPI_STORE, 128, 1, 1>(ta, tb, p, bound, st);
+  }
+  return MOE_ERR_ARG;
+}
+
+extern "C" int moe_fc1_swiglu_bf16(const void* xp, const void* w1, const int32_t* offsets,
+                                   const float* p_rows, int E, long long rows, int H, int F,
+                                   void* gu, void* h, moe_stream_t stream) {
+  if (!gemm_common_ok(xp, w1, gu, offsets, E) || !h || !aligned16(h) || !p_rows) return MOE_ERR_ARG;
+  if (H < BK || H % BK || F < 64 || F % 64 || rows < 0 || rows >= (1LL << 31)) return MOE_ERR_ARG;
+  if (rows == 0) return MOE_OK;
+  Params p{};
+  p.offsets = offsets;
+  p.E = E;
+  p.N = 2 * F;
+  p.K = H;
+  p.F = F;
+  p.p_rows = p_rows;
+  p.GU = static_cast<__nv_bfloat16*>(gu);
+  p.Hout = static_cast<__nv_bfloat16*>(h);
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, xp, kBF16, 2, rows, H, H, BM, BK)) return MOE_ERR_CUDA;
+  if (!make_tmap(&tb, w1, kBF16, 2, (long long)E * H, 2 * F, 2 * F, BK, 64)) return MOE_ERR_CUDA;
+  long long bound_base = rows / BM + E;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (F % 128 == 0)
+    return launch<FPROP, EPI_SWIGLU_FWD, 256, 0, 1>(ta, tb, p, bound_base * (F / 128), st);
+  return launch<FPROP, EPI_SWIGLU_FWD, 128, 0, 1>(ta, tb, p, bound_base * (F / 64), st);
+}
+
+extern "C" int moe_swiglu_bwd_parts(int F) {
+  if (F < 128 || F % 128) return 0;
+  return (F % 256 == 0) ? F / 256 : F / 128;
+}
+
+extern "C" int moe_fc2_dgrad_swiglu_bwd_bf16(const void* dy2, const void* w2,
+                                             const int32_t* offsets, const float* p_rows,
+                                             const void* gu, int E, long long rows, int H, int F,
+                                             void* dy1, float* dp_part, moe_stream_t stream) {
+  if (!gemm_common_ok(dy2, w2, dy1, offsets, E) || !gu || !aligned16(gu) || !p_rows || !dp_part)
+    return MOE_ERR_ARG;
+  if (H < BK || H % BK || F < 128 || F % 128 || rows < 0 || rows >= (1LL << 31)) return MOE_ERR_ARG;
+  if (rows == 0) return MOE_OK;
+  Params p{};
+  p.offsets = offsets;
+  p.E = E;
+  p.N = F;
+  p.K = H;
+  p.F = F;
+  p.p_rows = p_rows;
+  p.GU = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(gu));
+  p.C = static_cast<__nv_bfloat16*>(dy1);
+  p.ldc = 2LL * F;
+  p.dp_part = dp_part;
+  p.n_part = moe_swiglu_bwd_parts(F);
+  const bool bn256 = (F % 256) == 0;
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, dy2, kBF16, 2, rows, H, H, BM, BK)) return MOE_ERR_CUDA;
+  // dH = dY2 * W2_e^T: B_e = W2_e stored [F, H] = [N, K], K-major.
+  if (!make_tmap(&tb, w2, kBF16, 2, (long long)E * F, H, H, bn256 ? 128 : 64, BK))
+    return MOE_ERR_CUDA;
+  long long bound = (rows / BM + E) * (long long)(F / 128);
+  cudaStream_t st = (cudaStream_t)stream;
+  return bn256 ? launch<FPROP, EPI_SWIGLU_BWD, 256, 0, 0>(ta, tb, p, bound, st)
+               : launch<FPROP, EPI_SWIGLU_BWD, 128, 0, 0>(ta, tb, p, bound, st);
+}

@@ -1,0 +1,7 @@
+// Single translation unit of libmoe: every kernel file is included here so
+// that the device error word and other file-scope device symbols need no
+// relocatable device code.
+#include "route.cu"
+#include "permute.cu"
+#include "quant.cu"
+#include "gemm.cu"

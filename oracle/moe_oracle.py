@@ -523,3 +523,38 @@ def sampled_weight_grads(x, logits, W1, W2, dout, k, fcols, mx=False):
         dW1g[e] = x_col.T @ dg_col
         dW1u[e] = x_col.T @ du_col
     return {"dW1g": dW1g, "dW1u": dW1u, "dW2": dW2s}
+
+
+# ---------------------------------------------------------------------------
+# Grouped GEMM [EMT §Challenge 1: GroupedLinear over per-expert row groups]
+# ---------------------------------------------------------------------------
+
+def grouped_gemm_fprop(A, B, offsets, b_layout=0):
+    """C[r] = A[r] @ B_e for the rows r of group e (offsets[e] <= r < offsets[e+1]).
+
+    b_layout 0: B[e] is [K, N]; 1: B[e] is [N, K] (used transposed).
+    Rows outside every group are left zero.
+    """
+    A = np.asarray(A, dtype=f64)
+    B = np.asarray(B, dtype=f64)
+    offsets = np.asarray(offsets)
+    N = B.shape[2] if b_layout == 0 else B.shape[1]
+    C = np.zeros((A.shape[0], N))
+    for e in range(len(offsets) - 1):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        Be = B[e] if b_layout == 0 else B[e].T
+        C[r0:r1] = A[r0:r1] @ Be
+    return C
+
+
+def grouped_gemm_wgrad(A, B, offsets):
+    """C[e] = A[rows_e]^T @ B[rows_e]: the reduction runs over group e's rows."""
+    A = np.asarray(A, dtype=f64)
+    B = np.asarray(B, dtype=f64)
+    offsets = np.asarray(offsets)
+    E = len(offsets) - 1
+    C = np.zeros((E, A.shape[1], B.shape[1]))
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        C[e] = A[r0:r1].T @ B[r0:r1]
+    return C

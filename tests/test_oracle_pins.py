@@ -373,3 +373,25 @@ def test_planted_mistakes_are_caught(monkeypatch):
         m.setattr(O, "silu", lambda z: z)  # plain GLU instead of SwiGLU
         out = O.layer_forward(xs, np.zeros((3, 1)), W1s, W2s, 1)["out"]
     assert not np.allclose(out, _dense_swiglu_mlp(xs, W1s[0], W2s[0]))
+
+
+def test_grouped_gemm_brute_force():
+    rng = np.random.default_rng(19)
+    offsets = np.array([0, 3, 3, 7])
+    A = rng.standard_normal((8, 4))
+    B = rng.standard_normal((3, 4, 5))
+    C = O.grouped_gemm_fprop(A, B, offsets)
+    Ct = O.grouped_gemm_fprop(A, np.transpose(B, (0, 2, 1)).copy(), offsets, b_layout=1)
+    for r in range(8):
+        e = 0 if r < 3 else (2 if r < 7 else None)
+        for n in range(5):
+            want = 0.0 if e is None else sum(A[r, i] * B[e, i, n] for i in range(4))
+            assert abs(C[r, n] - want) < 1e-12 and abs(Ct[r, n] - want) < 1e-12
+    Y = rng.standard_normal((8, 6))
+    W = O.grouped_gemm_wgrad(A, Y, offsets)
+    assert np.all(W[1] == 0)
+    for e, (r0, r1) in enumerate([(0, 3), (3, 3), (3, 7)]):
+        for m in range(4):
+            for n in range(6):
+                want = sum(A[r, m] * Y[r, n] for r in range(r0, r1))
+                assert abs(W[e, m, n] - want) < 1e-12
