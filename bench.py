@@ -1,0 +1,490 @@
+"""Benchmark: MoE expert layer forward + backward on B300.
+
+One step = one pass of the whole layer (route, expert sort, permute, FC1 +
+scaled SwiGLU, FC2, combine, and the full backward) over one batch of T
+tokens, through the libmoe C ABI.
+
+Prints ONE JSON line (rank 0). Default: 1 GPU, the Mixtral-8x7B expert-layer
+workload in BF16 (T=8192, H=4096, F=14336, E=8, top-2).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Multi-GPU (launched with torch.distributed.run): each rank runs its own
+T-token batch (the layer is data-parallel over tokens; no collective is on
+the data path), so scaling is weak and `value` sums the tokens of all ranks
+over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_experts_expert_sort_b300 import inputs as I  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (fwd+bwd) and grouped-GEMM TFLOP/s, % of B300 peak"
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"],
+                "bf16_tflops_sustained": pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+                "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- the step
+
+class Step:
+    """The layer pass as the sequence of C-ABI calls (same order as
+    moe_layer_forward / moe_layer_backward), with optional CUDA events
+    between kernels for the per-kernel breakdown."""
+
+    NAMES = ["route", "plan", "permute_x", "fc1_swiglu", "fc2", "unpermute",
+             "permute_dout", "fc2_dgrad_swiglu_bwd", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad",
+             "unpermute_dx", "route_bwd"]
+
+    def __init__(self, wl, dev):
+        from mixture_experts_expert_sort_b300 import binding as B
+        from mixture_experts_expert_sort_b300.layer import MoELayer
+        self.B = B
+        self.wl = wl
+        self.layer = MoELayer(wl.T, wl.H, wl.F, wl.E, wl.k, precision="bf16", align=wl.align,
+                              device=dev)
+        L = self.layer
+        self.parts = {n: L.part(n) for n in ("idx", "w", "counts", "offsets", "dest", "src", "xp",
+                                             "gu", "h")}
+        self.rmax = B.moe_rows_padded_max(wl.T, wl.E, wl.k, wl.align)
+        R = self.rmax
+        bf = torch.bfloat16
+        self.p_rows = torch.empty(R, dtype=torch.float32, device=dev)
+        self.plan_ws = torch.empty(B.moe_permute_plan_workspace_size(wl.T, wl.E, wl.k),
+                                   dtype=torch.uint8, device=dev)
+        self.y2 = torch.empty((R, wl.H), dtype=bf, device=dev)
+        self.dy2 = torch.empty((R, wl.H), dtype=bf, device=dev)
+        self.dy1 = torch.empty((R, 2 * wl.F), dtype=bf, device=dev)
+        self.dxp = torch.empty((R, wl.H), dtype=bf, device=dev)
+        self.dp = torch.empty((R, B.moe_swiglu_bwd_parts(wl.F)), dtype=torch.float32, device=dev)
+        self.launches_per_step = 15
+
+    def run(self, logits, x, w1, w2, dout, out, dx, dw1, dw2, dlogits, ev=None):
+        B, wl, P = self.B, self.wl, self.parts
+        L = B.lib()
+        s = B.stream_handle()
+        T, H, F, E, k, R = wl.T, wl.H, wl.F, wl.E, wl.k, self.rmax
+        p = B.ptr
+        chk = B._check
+
+        def mark(i):
+            if ev is not None:
+                ev[i].record()
+        mark(0)
+        chk(L.moe_route(p(logits), T, E, k, p(P["idx"]), p(P["w"]), s), "route")
+        mark(1)
+        chk(L.moe_permute_plan(p(P["idx"]), T, E, k, wl.align, p(P["counts"]), p(P["offsets"]),
+                               p(P["dest"]), p(P["src"]), R, p(self.plan_ws),
+                               self.plan_ws.numel(), s), "plan")
+        mark(2)
+        chk(L.moe_permute(p(x), p(P["dest"]), p(P["offsets"]), p(P["counts"]), p(P["w"]), T, H, E,
+                          k, p(P["xp"]), p(self.p_rows), s), "permute")
+        mark(3)
+        chk(L.moe_fc1_swiglu_bf16(p(P["xp"]), p(w1), p(P["offsets"]), p(self.p_rows), E, R, H, F,
+                                  p(P["gu"]), p(P["h"]), s), "fc1")
+        mark(4)
+        chk(L.moe_grouped_gemm_bf16(0, p(P["h"]), p(w2), 0, p(P["offsets"]), E, R, 0, H, F,
+                                    p(self.y2), s), "fc2")
+        mark(5)
+        chk(L.moe_unpermute(p(self.y2), p(P["dest"]), None, T, H, k, p(out), s), "unpermute")
+        mark(6)
+        chk(L.moe_permute(p(dout), p(P["dest"]), p(P["offsets"]), p(P["counts"]), None, T, H, E,
+                          k, p(self.dy2), None, s), "permute dout")
+        mark(7)
+        chk(L.moe_fc2_dgrad_swiglu_bwd_bf16(p(self.dy2), p(w2), p(P["offsets"]), p(self.p_rows),
+                                            p(P["gu"]), E, R, H, F, p(self.dy1), p(self.dp), s),
+            "fc2 dgrad")
+        mark(8)
+        chk(L.moe_grouped_gemm_bf16(1, p(P["h"]), p(self.dy2), 0, p(P["offsets"]), E, R, F, H, 0,
+                                    p(dw2), s), "fc2 wgrad")
+        mark(9)
+        chk(L.moe_grouped_gemm_bf16(0, p(self.dy1), p(w1), 1, p(P["offsets"]), E, R, 0, H, 2 * F,
+                                    p(self.dxp), s), "fc1 dgrad")
+        mark(10)
+        chk(L.moe_grouped_gemm_bf16(1, p(P["xp"]), p(self.dy1), 0, p(P["offsets"]), E, R, H,
+                                    2 * F, 0, p(dw1), s), "fc1 wgrad")
+        mark(11)
+        chk(L.moe_unpermute(p(self.dxp), p(P["dest"]), None, T, H, k, p(dx), s), "unpermute dx")
+        mark(12)
+        nparts = self.dp.shape[1]
+        chk(L.moe_route_backward(p(self.dp), nparts, nparts, p(P["dest"]), p(P["w"]),
+                                 p(P["idx"]), T, E, k, p(dlogits), s), "route bwd")
+        mark(13)
+
+
+def kernel_work(wl):
+    """Algorithmic work per launch: flops for GEMMs, bytes for the rest."""
+    T, H, F, E, k = wl.T, wl.H, wl.F, wl.E, wl.k
+    R = T * k
+    g = {
+        "fc1_swiglu": ("flops", 4.0 * R * H * F),
+        "fc2": ("flops", 2.0 * R * H * F),
+        "fc2_dgrad_swiglu_bwd": ("flops", 2.0 * R * H * F),
+        "fc2_wgrad": ("flops", 2.0 * R * H * F),
+        "fc1_dgrad": ("flops", 4.0 * R * H * F),
+        "fc1_wgrad": ("flops", 4.0 * R * H * F),
+        "route": ("bytes", T * E * 4.0 + R * 8.0),
+        "plan": ("bytes", R * 4.0 * 3),
+        "permute_x": ("bytes", T * H * 2.0 + R * H * 2.0),
+        "unpermute": ("bytes", R * H * 2.0 + T * H * 2.0),
+        "permute_dout": ("bytes", T * H * 2.0 + R * H * 2.0),
+        "unpermute_dx": ("bytes", R * H * 2.0 + T * H * 2.0),
+        "route_bwd": ("bytes", R * 4.0 * 2 + T * E * 4.0),
+    }
+    return g
+
+
+# ------------------------------------------------------------ CPU oracle
+
+_ORACLE_INPUTS = {}
+
+
+def _oracle_inputs(wl, t_slice):
+    key = (wl.name, t_slice)
+    if key not in _ORACLE_INPUTS:
+        inp = I.make_all(wl.with_tokens(t_slice))
+        _ORACLE_INPUTS[key] = (inp["x"].float().numpy(), inp["logits"].numpy(),
+                               inp["w1"].float().numpy(), inp["w2"].float().numpy(),
+                               inp["dout"].float().numpy())
+    return _ORACLE_INPUTS[key]
+
+
+def oracle_sample_time(wl, t_slice):
+    """Time the oracle's per-expert loop, forward + backward, on the first
+    t_slice tokens of the workload (all experts, full width; inputs drawn
+    before the clock starts). Returns (seconds, tokens)."""
+    from oracle import moe_oracle as O
+    x, lg, w1, w2, dout = _oracle_inputs(wl, t_slice)
+    mx = wl.precision == "mxfp8"
+    t0 = time.perf_counter()
+    chk = 0.0
+    for e, tok, slot, y2, dxp, dp, dW1e, dW2e in O.layer_fwd_bwd_expert_stream(
+            x, lg, w1, w2, dout, wl.k, mx):
+        chk += float(dW1e[0, 0]) + float(y2.sum())
+    return time.perf_counter() - t0, t_slice
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def _set_blas_threads():
+    n = str(host_cores())
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ.setdefault(v, n)
+
+
+# ---------------------------------------------------------------- arms
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, wl, world, rank):
+    """The oracle, as it stands, on the host cores: a bounded token slice of
+    the workload per step."""
+    if rank != 0:
+        return
+    _set_blas_threads()
+    t_slice = args.ref_tokens
+    for _ in range(min(args.warmup, 1)):
+        oracle_sample_time(wl, t_slice)
+    times = []
+    for _ in range(args.steps):
+        dt, n = oracle_sample_time(wl, t_slice)
+        times.append(dt)
+    tot = sum(times)
+    value = t_slice * args.steps / tot
+    cores = host_cores()
+    sample = (f"first {t_slice} tokens of the {wl.name} workload per step "
+              f"(all {wl.E} experts, full H={wl.H}, F={wl.F}), fwd+bwd, fp64")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * tot / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl),
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl):
+    return {"workload": f"{wl.name}: MoE expert layer T={wl.T} H={wl.H} F={wl.F} E={wl.E} "
+                        f"top-{wl.k} {wl.precision.upper()} fwd+bwd",
+            "T": wl.T, "H": wl.H, "F": wl.F, "E": wl.E, "k": wl.k, "precision": wl.precision,
+            "global_batch_tokens": wl.T,
+            "l2": "inputs larger than L2 (weights alone 2*E*H*F*3 bytes per step)"}
+
+
+def run_ours(args, wl, world, rank, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from mixture_experts_expert_sort_b300 import binding as B
+    B.lib()
+    # Seeded synthetic inputs generated on the device (rank-distinct seeds).
+    wlr = wl if rank == 0 else I.Workload(wl.name, wl.T, wl.H, wl.F, wl.E, wl.k, wl.precision,
+                                          wl.seed + 100 * rank, wl.zipf_s, wl.zero_experts,
+                                          wl.outlier_frac)
+    inp = I.make_all(wlr, device=dev)
+    logits, x, w1, w2, dout = inp["logits"], inp["x"], inp["w1"], inp["w2"], inp["dout"]
+    T, H, F, E = wl.T, wl.H, wl.F, wl.E
+    bf = torch.bfloat16
+    out = torch.empty((T, H), dtype=bf, device=dev)
+    dx = torch.empty((T, H), dtype=bf, device=dev)
+    dw1 = torch.empty((E, H, 2 * F), dtype=bf, device=dev)
+    dw2 = torch.empty((E, F, H), dtype=bf, device=dev)
+    dlogits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    step = Step(wl, dev)
+    args_run = (logits, x, w1, w2, dout, out, dx, dw1, dw2, dlogits)
+
+    for _ in range(args.warmup):
+        step.run(*args_run)
+    torch.cuda.synchronize()
+    if B.device_error() != 0:
+        raise RuntimeError("device error flag set during warm-up")
+
+    # ---- timed region: K steps, per-kernel events on the launching stream
+    nk = len(Step.NAMES)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(args.steps):
+        step.run(*args_run, ev=evs[i])
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    ms = max_over_ranks(ms, world)
+    per_kernel = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1])
+                                     for i in range(args.steps))
+                  for j, n in enumerate(Step.NAMES)}
+    if B.device_error() != 0:
+        raise RuntimeError("device error flag set during the timed region")
+
+    # ---- end to end through the public layer API with host buffers
+    layer = step.layer
+    h_x = x.cpu().pin_memory()
+    h_lg = logits.cpu().pin_memory()
+    h_do = dout.cpu().pin_memory()
+    d_x = torch.empty_like(x)
+    d_lg = torch.empty_like(logits)
+    d_do = torch.empty_like(dout)
+    h_out = torch.empty((T, H), dtype=bf).pin_memory()
+    h_dx = torch.empty((T, H), dtype=bf).pin_memory()
+    h_dl = torch.empty((T, E), dtype=torch.float32).pin_memory()
+    e2e_steps = max(1, min(args.steps, 10))
+
+    def e2e_step():
+        d_x.copy_(h_x, non_blocking=True)
+        d_lg.copy_(h_lg, non_blocking=True)
+        d_do.copy_(h_do, non_blocking=True)
+        layer.forward(d_lg, d_x, w1, w2, out=out)
+        layer.backward(d_do, w1, w2, dx=dx, dw1=dw1, dw2=dw2, dlogits=dlogits)
+        h_out.copy_(out, non_blocking=True)
+        h_dx.copy_(dx, non_blocking=True)
+        h_dl.copy_(dlogits, non_blocking=True)
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    a1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1) / e2e_steps, world)
+    h2d = h_x.numel() * 2 + h_lg.numel() * 4 + h_do.numel() * 2
+    d2h = h_out.numel() * 2 + h_dx.numel() * 2 + h_dl.numel() * 4
+
+    if rank != 0:
+        return
+    peaks = load_peaks()
+    ms_step = ms / args.steps
+    tokens_per_s = world * T / (ms_step / 1000.0)
+    work = kernel_work(wl)
+    gemm_names = [n for n, (kind, _) in work.items() if kind == "flops"]
+    gemm_ms = sum(per_kernel[n] for n in gemm_names)
+    gemm_tflops = wl.gemm_flops_fwd_bwd() / (gemm_ms / 1000.0) / 1e12
+    dom = max(per_kernel, key=lambda n: per_kernel[n])
+    kind, amount = work[dom]
+    if kind == "flops":
+        ach = amount / (per_kernel[dom] / 1000.0) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": None, "kernel": dom,
+                "peak_kind": f"bf16 sustained ({peaks['source']})"}
+    else:
+        ach = amount / (per_kernel[dom] / 1000.0) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                "traffic": None, "kernel": dom, "peak_kind": f"hbm copy ({peaks['source']})"}
+    kern = {}
+    for n in Step.NAMES:
+        kind, amount = work[n]
+        t = per_kernel[n] / 1000.0
+        kern[n] = {"ms": round(per_kernel[n], 4),
+                   ("tflops" if kind == "flops" else "gbs"):
+                       round(amount / t / (1e12 if kind == "flops" else 1e9), 1)}
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded, generated on the device)",
+        "config": config_of(wl),
+        "gemm_tflops": gemm_tflops,
+        "gemm_frac_of_bf16_sustained": gemm_tflops / peaks["bf16_tflops_sustained"],
+        "gemm_frac_of_bf16_spec_2250": gemm_tflops / 2250.0,
+        "roofline": roof,
+        "e2e": {"value": world * T / (e2e_ms / 1000.0), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "moe_layer_forward + moe_layer_backward, host pinned inputs/outputs"},
+        "gpu_launches": step.launches_per_step * args.steps,
+        "clocks": clk,
+        "kernels": kern,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        _set_blas_threads()
+        dt, n = oracle_sample_time(wl, args.cpu_tokens)
+        line["cpu_baseline"] = {
+            "value": n / dt, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+            "sample": f"first {n} tokens of the workload, all experts, full width, fwd+bwd, fp64"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="mixtral", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=256)
+    ap.add_argument("--ref-tokens", type=int, default=128)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    wl = I.WORKLOADS[args.workload]
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, wl, world, rank)
+    else:
+        run_ours(args, wl, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -235,6 +235,55 @@ MOE_API int moe_fc2_dgrad_swiglu_bwd_bf16(const void* dy2, const void* w2,
                                           const void* gu, int E, long long rows, int H, int F,
                                           void* dy1, float* dp_part, moe_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * The whole layer ("Efficient MoE Training ...", §Challenge 1 per-expert
+ * loop, §Challenge 3 fused gate_up -> ScaledSwiGLU -> down), forward and
+ * backward, as one call each over a caller-owned device workspace that also
+ * carries the state saved between the two calls.
+ *
+ * Forward:  out[t] = sum_j w[t,j] * (silu(x W1_e[:, :F]) * (x W1_e[:, F:])) W2_e,
+ *           e = idx[t, j] from moe_route(logits).
+ *   logits [T, E] fp32; x [T, H] bf16; w1 [E, H, 2F] bf16 (gate | up);
+ *   w2 [E, F, H] bf16; out [T, H] bf16.
+ * Backward: gradients of L = sum(out * dout):
+ *   dx [T, H] bf16, dw1 [E, H, 2F] bf16, dw2 [E, F, H] bf16,
+ *   dlogits [T, E] fp32 (through the top-k softmax weights only).
+ *   Must follow moe_layer_forward with the same cfg, weights and workspace.
+ * Requirements: H % 128 == 0, F % 128 == 0, 1 <= k <= 8, k <= E <= 256,
+ * align a multiple of 128 (groups are padded with zero rows), precision
+ * MOE_PRECISION_BF16. moe_layer_workspace_size returns 0 for an unsupported
+ * cfg. The workspace must be 256-byte aligned.
+ * moe_layer_workspace_part gives the byte offset and size of one saved
+ * intermediate (MOE_PART_*) inside the workspace, for inspection.
+ */
+#define MOE_PRECISION_BF16 0
+#define MOE_PRECISION_MXFP8 1
+typedef struct moe_layer_config {
+  int T, H, F, E, k;
+  int align;
+  int precision;
+} moe_layer_config;
+
+#define MOE_PART_IDX 0      /* int32 [T, k] */
+#define MOE_PART_W 1        /* fp32 [T, k] */
+#define MOE_PART_COUNTS 2   /* int32 [E] */
+#define MOE_PART_OFFSETS 3  /* int32 [E + 1] */
+#define MOE_PART_DEST 4     /* int32 [T * k] */
+#define MOE_PART_SRC 5      /* int32 [R_max] */
+#define MOE_PART_XP 8       /* bf16 [R_max, H] */
+#define MOE_PART_GU 9       /* bf16 [R_max, 2F] */
+#define MOE_PART_H 10       /* bf16 [R_max, F] */
+
+MOE_API size_t moe_layer_workspace_size(const moe_layer_config* cfg);
+MOE_API int moe_layer_workspace_part(const moe_layer_config* cfg, int part, size_t* offset,
+                                     size_t* bytes);
+MOE_API int moe_layer_forward(const moe_layer_config* cfg, const float* logits, const void* x,
+                              const void* w1, const void* w2, void* out, void* workspace,
+                              size_t workspace_bytes, moe_stream_t stream);
+MOE_API int moe_layer_backward(const moe_layer_config* cfg, const void* dout, const void* w1,
+                               const void* w2, void* dx, void* dw1, void* dw2, float* dlogits,
+                               void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -40,6 +40,10 @@ SIGNATURES = {
     "moe_fc1_swiglu_bf16": (_i, [_p, _p, _p, _p, _i, _ll, _i, _i, _p, _p, _p]),
     "moe_swiglu_bwd_parts": (_i, [_i]),
     "moe_fc2_dgrad_swiglu_bwd_bf16": (_i, [_p, _p, _p, _p, _p, _i, _ll, _i, _i, _p, _p, _p]),
+    "moe_layer_workspace_size": (_sz, [_p]),
+    "moe_layer_workspace_part": (_i, [_p, _i, C.POINTER(_sz), C.POINTER(_sz)]),
+    "moe_layer_forward": (_i, [_p, _p, _p, _p, _p, _p, _p, _sz, _p]),
+    "moe_layer_backward": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
 }
 
 
@@ -238,3 +242,45 @@ def moe_fc2_dgrad_swiglu_bwd_bf16(dy2, w2, offsets, p_rows, gu, dy1=None, dp_par
                                                stream_handle(stream)),
            "moe_fc2_dgrad_swiglu_bwd_bf16")
     return dy1, dp_part
+
+
+# ------------------------------------------------------------- whole layer
+
+PRECISION = {"bf16": 0, "mxfp8": 1}
+PARTS = {"idx": (0, torch.int32), "w": (1, torch.float32), "counts": (2, torch.int32),
+         "offsets": (3, torch.int32), "dest": (4, torch.int32), "src": (5, torch.int32),
+         "xp": (8, torch.bfloat16), "gu": (9, torch.bfloat16), "h": (10, torch.bfloat16)}
+
+
+class LayerConfig(C.Structure):
+    _fields_ = [("T", C.c_int), ("H", C.c_int), ("F", C.c_int), ("E", C.c_int), ("k", C.c_int),
+                ("align", C.c_int), ("precision", C.c_int)]
+
+
+def layer_config(T, H, F, E, k, precision="bf16", align=128):
+    return LayerConfig(T, H, F, E, k, align, PRECISION[precision])
+
+
+def moe_layer_workspace_size(cfg):
+    return int(lib().moe_layer_workspace_size(C.byref(cfg)))
+
+
+def moe_layer_workspace_part(cfg, part):
+    off, nb = _sz(0), _sz(0)
+    _check(lib().moe_layer_workspace_part(C.byref(cfg), part, C.byref(off), C.byref(nb)),
+           "moe_layer_workspace_part")
+    return off.value, nb.value
+
+
+def moe_layer_forward(cfg, logits, x, w1, w2, out, workspace, stream=None):
+    _check(lib().moe_layer_forward(C.byref(cfg), ptr(logits), ptr(x), ptr(w1), ptr(w2), ptr(out),
+                                   ptr(workspace), workspace.numel(), stream_handle(stream)),
+           "moe_layer_forward")
+    return out
+
+
+def moe_layer_backward(cfg, dout, w1, w2, dx, dw1, dw2, dlogits, workspace, stream=None):
+    _check(lib().moe_layer_backward(C.byref(cfg), ptr(dout), ptr(w1), ptr(w2), ptr(dx), ptr(dw1),
+                                    ptr(dw2), ptr(dlogits), ptr(workspace), workspace.numel(),
+                                    stream_handle(stream)), "moe_layer_backward")
+    return dx, dw1, dw2, dlogits

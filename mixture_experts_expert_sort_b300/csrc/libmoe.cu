@@ -5,3 +5,4 @@
 #include "permute.cu"
 #include "quant.cu"
 #include "gemm.cu"
+#include "layer.cu"

@@ -1,0 +1,45 @@
+"""MoELayer: owns the device workspace of one layer shape and calls the
+library's whole-layer forward and backward (argument marshalling only)."""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+class MoELayer:
+    def __init__(self, T, H, F, E, k, precision="bf16", align=128, device="cuda"):
+        self.T, self.H, self.F, self.E, self.k = T, H, F, E, k
+        self.precision = precision
+        self.cfg = B.layer_config(T, H, F, E, k, precision, align)
+        nbytes = B.moe_layer_workspace_size(self.cfg)
+        if nbytes == 0:
+            raise B.MoeError(f"unsupported layer config T={T} H={H} F={F} E={E} k={k} "
+                             f"precision={precision} align={align}")
+        self.device = torch.device(device)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+
+    def forward(self, logits, x, w1, w2, out=None, stream=None):
+        out = out if out is not None else torch.empty((self.T, self.H), dtype=torch.bfloat16,
+                                                      device=self.device)
+        return B.moe_layer_forward(self.cfg, logits, x, w1, w2, out, self.workspace, stream)
+
+    def backward(self, dout, w1, w2, dx=None, dw1=None, dw2=None, dlogits=None, stream=None):
+        dev = self.device
+        dx = dx if dx is not None else torch.empty((self.T, self.H), dtype=torch.bfloat16,
+                                                   device=dev)
+        dw1 = dw1 if dw1 is not None else torch.empty((self.E, self.H, 2 * self.F),
+                                                      dtype=torch.bfloat16, device=dev)
+        dw2 = dw2 if dw2 is not None else torch.empty((self.E, self.F, self.H),
+                                                      dtype=torch.bfloat16, device=dev)
+        dlogits = dlogits if dlogits is not None else torch.empty((self.T, self.E),
+                                                                  dtype=torch.float32, device=dev)
+        return B.moe_layer_backward(self.cfg, dout, w1, w2, dx, dw1, dw2, dlogits, self.workspace,
+                                    stream)
+
+    def part(self, name):
+        """A typed view of one saved intermediate in the workspace."""
+        pid, dtype = B.PARTS[name]
+        off, nbytes = B.moe_layer_workspace_part(self.cfg, pid)
+        esz = torch.empty((), dtype=dtype).element_size()
+        return self.workspace[off:off + nbytes].view(dtype)[: nbytes // esz]
