@@ -474,8 +474,15 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=256)
     ap.add_argument("--ref-tokens", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (profiling cases)")
+    ap.add_argument("--experts", type=int, default=0, help="override E (profiling cases)")
     args = ap.parse_args()
     wl = I.WORKLOADS[args.workload]
+    if args.tokens or args.experts:
+        # A reduced case of the same layer shape (H, F, k kept), for profiling.
+        wl = I.Workload(wl.name + "_reduced", args.tokens or wl.T, wl.H, wl.F,
+                        args.experts or wl.E, wl.k, wl.precision, wl.seed, wl.zipf_s,
+                        wl.zero_experts, wl.outlier_frac)
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, wl, world, rank)
