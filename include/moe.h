@@ -127,6 +127,29 @@ MOE_API int moe_permute_plan(const int32_t* idx, int T, int E, int k, int align,
                      int32_t* offsets, int32_t* dest, int32_t* src, long long src_rows,
                      void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* moe_permute_plan_static: moe_permute_plan for callers that cannot
+ * allocate device memory (engines that give a plugin no workspace and forbid
+ * allocation after start-up, or latency-critical loops that cannot afford
+ * cudaMalloc's implicit device synchronisation). The sources have no
+ * counterpart of this call; it exists only for such callers.
+ *   Arguments and results are those of moe_permute_plan, without the
+ *   workspace: the scratch is a fixed array of MOE_PLAN_STATIC_SCRATCH_INTS
+ *   int32 (1 MiB) inside the library, held on every GPU that loads the
+ *   library until the process exits. The caller still passes all inputs and
+ *   outputs; nothing is allocated.
+ *   Limit: ceil(T*k / 1024) * E <= MOE_PLAN_STATIC_SCRATCH_INTS, else
+ *   MOE_ERR_UNSUPPORTED and nothing is enqueued.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   Every call shares the array: calls that overlap on the GPU (other
+ *   streams, threads) race and must be serialised by the caller. Each call
+ *   overwrites the scratch it reads, so nothing carries over between calls.
+ */
+#define MOE_PLAN_STATIC_SCRATCH_INTS 262144
+MOE_API int moe_permute_plan_static(const int32_t* idx, int T, int E, int k, int align,
+                                    int32_t* counts, int32_t* offsets, int32_t* dest,
+                                    int32_t* src, long long src_rows, moe_stream_t stream);
+
 /* moe_permute: the gather that makes each expert's rows contiguous
  * ("Efficient MoE Training ...", §Challenge 1, GroupedLinear "gathering ...
  * input tokens"): xp[dest[t*k + j]] = x[t]; padding rows

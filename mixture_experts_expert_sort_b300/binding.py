@@ -33,6 +33,7 @@ SIGNATURES = {
     "moe_rows_padded_max": (_ll, [_i, _i, _i, _i]),
     "moe_permute_plan_workspace_size": (_sz, [_i, _i, _i]),
     "moe_permute_plan": (_i, [_p, _i, _i, _i, _i, _p, _p, _p, _p, _ll, _p, _sz, _p]),
+    "moe_permute_plan_static": (_i, [_p, _i, _i, _i, _i, _p, _p, _p, _p, _ll, _p]),
     "moe_permute": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _p, _p, _p]),
     "moe_unpermute": (_i, [_p, _p, _p, _i, _i, _i, _p, _p]),
     "mxfp8_quantize": (_i, [_p, _ll, _i, _ll, _p, _i, _i, _p, _p, _p, _p, _p]),
@@ -143,6 +144,34 @@ def moe_permute_plan(idx, E, align, src_rows=None, workspace=None, stream=None, 
                                   ptr(out["offsets"]), ptr(out["dest"]), ptr(out["src"]),
                                   src_rows, ptr(workspace), workspace.numel(),
                                   stream_handle(stream)), "moe_permute_plan")
+    return out
+
+
+PLAN_STATIC_SCRATCH_INTS = 262144
+
+
+def moe_permute_plan_static(idx, E, align, src_rows=None, stream=None, out=None):
+    """moe_permute_plan without a workspace, for callers that cannot allocate
+    device memory: the library's fixed 1 MiB scratch array is used instead.
+    Raises MoeError when ceil(T*k/1024)*E exceeds that array."""
+    T, k = idx.shape
+    dev = idx.device
+    src_rows = moe_rows_padded_max(T, E, k, align) if src_rows is None else src_rows
+    if out is None:
+        out = {
+            "counts": torch.empty(E, dtype=torch.int32, device=dev),
+            "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+            "dest": torch.empty(max(T * k, 1), dtype=torch.int32, device=dev),
+            "src": torch.empty(max(src_rows, 1), dtype=torch.int32, device=dev),
+        }
+    st = lib().moe_permute_plan_static(ptr(idx), T, E, k, align, ptr(out["counts"]),
+                                       ptr(out["offsets"]), ptr(out["dest"]), ptr(out["src"]),
+                                       src_rows, stream_handle(stream))
+    if st == MOE_ERR_UNSUPPORTED:
+        raise MoeError(f"moe_permute_plan_static: ceil(T*k/1024)*E = "
+                       f"{-(-T * k // 1024) * E} exceeds the static scratch of "
+                       f"{PLAN_STATIC_SCRATCH_INTS} int32")
+    _check(st, "moe_permute_plan_static")
     return out
 
 

@@ -3,6 +3,7 @@
 // relocatable device code.
 #include "route.cu"
 #include "permute.cu"
+#include "plan_static.cu"
 #include "quant.cu"
 #include "gemm.cu"
 #include "layer.cu"
