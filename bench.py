@@ -312,6 +312,29 @@ def run_reference(args, wl, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def gemm_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "ptx.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "mixture_experts_expert_sort_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel, wl):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when there is none for this workload or the kernel source changed
+    since the counters were taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f).get(kernel)
+    except Exception:
+        return None
+    if not t or t.get("workload") != wl.name or t.get("source_sha256_16") != gemm_source_hash():
+        return None
+    return t["bytes_per_launch"]
+
+
 def config_of(wl):
     return {"workload": f"{wl.name}: MoE expert layer T={wl.T} H={wl.H} F={wl.F} E={wl.E} "
                         f"top-{wl.k} {wl.precision.upper()} fwd+bwd",
@@ -431,6 +454,7 @@ def run_ours(args, wl, world, rank, local):
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
                 "traffic": None, "kernel": dom, "peak_kind": f"hbm copy ({peaks['source']})"}
+    roof["traffic"] = measured_traffic(dom, wl)
     kern = {}
     for n in Step.NAMES:
         kind, amount = work[n]
