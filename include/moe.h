@@ -259,6 +259,67 @@ MOE_API int moe_fc2_dgrad_swiglu_bwd_bf16(const void* dy2, const void* w2,
                                           void* dy1, float* dp_part, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * MXFP8 grouped GEMMs on the block-scaled tcgen05 MMA ("Efficient MoE
+ * Training ...", §Challenge 2: MXFP8 GEMMs on Blackwell's block-scaled
+ * tensor-core instructions; §Challenge 3: the fused grouped MLP with
+ * quantisation folded in). Every operand is an MXFP8 tensor as written by
+ * mxfp8_quantize: E4M3 data [MN, K] with K contiguous and the tiled scale
+ * layout, with 32-blocks along the reduction dimension K. Accumulation is
+ * fp32; the result is the exact dot product of the dequantised operands up to
+ * fp32 summation order.
+ *
+ * moe_grouped_gemm_mxfp8, mode MOE_GEMM_FPROP:
+ *   C[r, n] = sum_k A[r, k] * B_e[n, k] for every row r of group e, with
+ *   B_e[n, k] = B[e*b_row_stride + n, e*b_k_stride + k]: a row-wise copy of
+ *   per-expert [N, K] weights uses (b_row_stride = N, b_k_stride = 0); a
+ *   column-wise copy of per-expert [K, N] weights, stored [N, E*K], uses
+ *   (0, K). A is [a_rows, a_cols = K], C [a_rows, N] bf16. N % 128 == 0
+ *   (a tail of 128 columns past a multiple of 256 is masked), K % 128 == 0.
+ * mode MOE_GEMM_WGRAD:
+ *   C_e[m, n] = sum over rows r of group e of A[m, r] * B[n, r] with A
+ *   [M, a_cols] and B [N, b_cols] the column-wise (transposed) copies,
+ *   a_cols = b_cols = rows. C = E x [M, N] bf16. M % 128 == 0, N % 256 == 0.
+ * All a_rows, a_cols, b_rows, b_cols are multiples of 128; group offsets
+ * must be multiples of 128 (else MOE_DEVERR_LAYOUT). */
+MOE_API int moe_grouped_gemm_mxfp8(int mode, const uint8_t* a, const uint8_t* sa,
+                                   long long a_rows, long long a_cols, const uint8_t* b,
+                                   const uint8_t* sb, long long b_rows, long long b_cols,
+                                   long long b_row_stride, long long b_k_stride,
+                                   const int32_t* offsets, int E, int M, int N, int K, void* C,
+                                   moe_stream_t stream);
+
+/* moe_fc1_swiglu_mxfp8: FC1 + ScaledSwiGLU + requantisation, MXFP8.
+ *   xq, sx: row-wise MXFP8 of the permuted tokens [rows, H].
+ *   w1t, sw1t: column-wise MXFP8 of W1 viewed as [E*H, 2F], i.e. data
+ *   [2F, E*H] (blocks along H).
+ *   For every row r of group e: [g | u] = x_r * W1_e (fp32),
+ *   gu[r] = [g | u] in bf16, h = silu(g)*u*p_rows[r] (fp32), written as
+ *   row-wise MXFP8 hq_row [rows, F] + sh_row and column-wise MXFP8 (blocks of
+ *   32 rows, transposed) hq_col [F, rows] + sh_col.
+ * Requires rows, H, F multiples of 128. */
+MOE_API int moe_fc1_swiglu_mxfp8(const uint8_t* xq, const uint8_t* sx, long long rows, int H,
+                                 const uint8_t* w1t, const uint8_t* sw1t, const int32_t* offsets,
+                                 const float* p_rows, int E, int F, void* gu, uint8_t* hq_row,
+                                 uint8_t* sh_row, uint8_t* hq_col, uint8_t* sh_col,
+                                 moe_stream_t stream);
+
+/* moe_fc2_dgrad_swiglu_bwd_mxfp8: FC2 dgrad + SwiGLU backward, MXFP8.
+ *   dy2q, sdy2: row-wise MXFP8 of the permuted upstream gradient [rows, H].
+ *   w2q, sw2: row-wise MXFP8 of W2 viewed as [E*F, H] (blocks along H).
+ *   dH = dy2 * W2_e^T; with g, u from gu and p = p_rows[r]:
+ *   dY1 = [dA*u*silu'(g) | dA*silu(g)] (dA = dH*p) written as row-wise MXFP8
+ *   dy1q_row [rows, 2F] + sdy1_row and column-wise dy1q_col [2F, rows] +
+ *   sdy1_col; dp_part[r, c] (c < ceil(F/256)) partial sums of dH*silu(g)*u.
+ * Requires rows, H, F multiples of 128. */
+MOE_API int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t* sdy2,
+                                           long long rows, int H, const uint8_t* w2q,
+                                           const uint8_t* sw2, const int32_t* offsets,
+                                           const float* p_rows, const void* gu, int E, int F,
+                                           uint8_t* dy1q_row, uint8_t* sdy1_row,
+                                           uint8_t* dy1q_col, uint8_t* sdy1_col, float* dp_part,
+                                           moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * The whole layer ("Efficient MoE Training ...", §Challenge 1 per-expert
  * loop, §Challenge 3 fused gate_up -> ScaledSwiGLU -> down), forward and
  * backward, as one call each over a caller-owned device workspace that also

@@ -41,6 +41,12 @@ SIGNATURES = {
     "moe_fc1_swiglu_bf16": (_i, [_p, _p, _p, _p, _i, _ll, _i, _i, _p, _p, _p]),
     "moe_swiglu_bwd_parts": (_i, [_i]),
     "moe_fc2_dgrad_swiglu_bwd_bf16": (_i, [_p, _p, _p, _p, _p, _i, _ll, _i, _i, _p, _p, _p]),
+    "moe_grouped_gemm_mxfp8": (_i, [_i, _p, _p, _ll, _ll, _p, _p, _ll, _ll, _ll, _ll, _p, _i,
+                                    _i, _i, _i, _p, _p]),
+    "moe_fc1_swiglu_mxfp8": (_i, [_p, _p, _ll, _i, _p, _p, _p, _p, _i, _i, _p, _p, _p, _p, _p,
+                                  _p]),
+    "moe_fc2_dgrad_swiglu_bwd_mxfp8": (_i, [_p, _p, _ll, _i, _p, _p, _p, _p, _p, _i, _i, _p, _p,
+                                            _p, _p, _p, _p]),
     "moe_layer_workspace_size": (_sz, [_p]),
     "moe_layer_workspace_part": (_i, [_p, _i, C.POINTER(_sz), C.POINTER(_sz)]),
     "moe_layer_forward": (_i, [_p, _p, _p, _p, _p, _p, _p, _sz, _p]),
@@ -271,6 +277,61 @@ def moe_fc2_dgrad_swiglu_bwd_bf16(dy2, w2, offsets, p_rows, gu, dy1=None, dp_par
                                                stream_handle(stream)),
            "moe_fc2_dgrad_swiglu_bwd_bf16")
     return dy1, dp_part
+
+
+# ----------------------------------------------------- MXFP8 grouped GEMM
+
+def moe_grouped_gemm_mxfp8(mode, a, sa, b, sb, offsets, b_row_stride=0, b_k_stride=0, M=0, N=0,
+                           K=0, C=None, stream=None):
+    """a, b: uint8 E4M3 data [rows, cols] (K-major); sa, sb: tiled scales."""
+    E = offsets.numel() - 1
+    a_rows, a_cols = a.shape
+    b_rows, b_cols = b.shape
+    if C is None:
+        shape = (a_rows, N) if mode == GEMM_FPROP else (E, M, N)
+        C = torch.empty(shape, dtype=torch.bfloat16, device=a.device)
+    _check(lib().moe_grouped_gemm_mxfp8(mode, ptr(a), ptr(sa), a_rows, a_cols, ptr(b), ptr(sb),
+                                        b_rows, b_cols, b_row_stride, b_k_stride, ptr(offsets), E,
+                                        M, N, K, ptr(C), stream_handle(stream)),
+           "moe_grouped_gemm_mxfp8")
+    return C
+
+
+def moe_fc1_swiglu_mxfp8(xq, sx, w1t, sw1t, offsets, p_rows, F, stream=None, out=None):
+    rows, H = xq.shape
+    E = offsets.numel() - 1
+    dev = xq.device
+    if out is None:
+        out = {"gu": torch.empty((rows, 2 * F), dtype=torch.bfloat16, device=dev),
+               "q_row": torch.empty((rows, F), dtype=torch.uint8, device=dev),
+               "s_row": torch.empty(mx_scale_bytes(rows, F), dtype=torch.uint8, device=dev),
+               "q_col": torch.empty((F, rows), dtype=torch.uint8, device=dev),
+               "s_col": torch.empty(mx_scale_bytes(F, rows), dtype=torch.uint8, device=dev)}
+    _check(lib().moe_fc1_swiglu_mxfp8(ptr(xq), ptr(sx), rows, H, ptr(w1t), ptr(sw1t), ptr(offsets),
+                                      ptr(p_rows), E, F, ptr(out["gu"]), ptr(out["q_row"]),
+                                      ptr(out["s_row"]), ptr(out["q_col"]), ptr(out["s_col"]),
+                                      stream_handle(stream)), "moe_fc1_swiglu_mxfp8")
+    return out
+
+
+def moe_fc2_dgrad_swiglu_bwd_mxfp8(dy2q, sdy2, w2q, sw2, offsets, p_rows, gu, F, stream=None,
+                                   out=None):
+    rows, H = dy2q.shape
+    E = offsets.numel() - 1
+    dev = dy2q.device
+    if out is None:
+        out = {"q_row": torch.empty((rows, 2 * F), dtype=torch.uint8, device=dev),
+               "s_row": torch.empty(mx_scale_bytes(rows, 2 * F), dtype=torch.uint8, device=dev),
+               "q_col": torch.empty((2 * F, rows), dtype=torch.uint8, device=dev),
+               "s_col": torch.empty(mx_scale_bytes(2 * F, rows), dtype=torch.uint8, device=dev),
+               "dp": torch.empty((rows, -(-F // 256)), dtype=torch.float32, device=dev)}
+    _check(lib().moe_fc2_dgrad_swiglu_bwd_mxfp8(ptr(dy2q), ptr(sdy2), rows, H, ptr(w2q), ptr(sw2),
+                                                ptr(offsets), ptr(p_rows), ptr(gu), E, F,
+                                                ptr(out["q_row"]), ptr(out["s_row"]),
+                                                ptr(out["q_col"]), ptr(out["s_col"]),
+                                                ptr(out["dp"]), stream_handle(stream)),
+           "moe_fc2_dgrad_swiglu_bwd_mxfp8")
+    return out
 
 
 # ------------------------------------------------------------- whole layer

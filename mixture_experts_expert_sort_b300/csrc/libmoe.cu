@@ -7,3 +7,4 @@
 #include "quant.cu"
 #include "gemm.cu"
 #include "layer.cu"
+#include "gemm_mx.cu"
