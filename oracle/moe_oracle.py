@@ -43,7 +43,13 @@ Readings where the sources are silent (each is repeated in the design notes):
   reduction dimension (row-wise for forward and dgrad, column-wise, i.e.
   along tokens inside an expert group, for wgrad); intermediate activations
   are rounded to float32 before they are quantised; the elementwise
-  backward is straight-through.
+  backward is straight-through;
+* in MXFP8 mode the SwiGLU backward works from the gate/up values that the
+  forward saved in BF16: [EMT §Challenge 3] has each low-precision GEMM's
+  result converted back to the 16-bit format, and the values this step
+  produces decide quantised codes, so the oracle takes that decision from
+  the same BF16 inputs as the kernel. The forward SwiGLU consumes the GEMM
+  result unrounded (the fused path folds the conversion into the epilogue).
 """
 from __future__ import annotations
 
@@ -260,6 +266,27 @@ def to_f32(a):
     return np.asarray(a, dtype=np.float32).astype(f64)
 
 
+def to_bf16(a):
+    """Round to float32, then to bfloat16 (8 exponent, 7 fraction bits) with
+    round-to-nearest-even on the 16 discarded bits, returned as float64.
+
+    Adding 0x7FFF plus the lowest kept bit to the float32 bit pattern and
+    clearing the low 16 bits rounds the magnitude to nearest, ties to even;
+    a carry into the exponent field is the correct rounding up to the next
+    binade (and to infinity past the largest finite value). NaN stays NaN.
+    """
+    x = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    u = x.view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    r = np.where(np.isnan(x), u | 0x00400000, r).astype(np.uint32)
+    return r.view(np.float32).astype(f64)
+
+
+def saved_gate_up(g, u, mx):
+    """Gate and up values the backward reads: BF16-saved in MXFP8 mode."""
+    return (to_bf16(g), to_bf16(u)) if mx else (g, u)
+
+
 # ---------------------------------------------------------------------------
 # Expert MLP [EMT §Challenge 1 GroupedLinear gate_up; §Challenge 3 ScaledSwiGLU, down]
 # ---------------------------------------------------------------------------
@@ -328,7 +355,8 @@ def expert_backward(xe, p, W1e, W2e, dy2, saved, mx=False):
     dW2 = H^T @ dY2; dXp = dY1 @ W1^T; dW1 = Xp^T @ dY1.
     Returns (dxp [n, H], dp [n], dW1e [H, 2F], dW2e [F, H]).
     """
-    g, u, h = saved["g"], saved["u"], saved["h"]
+    g, u = saved_gate_up(saved["g"], saved["u"], mx)
+    h = saved["h"]
     p = np.asarray(p, dtype=f64)[:, None]
     dy2 = np.asarray(dy2, dtype=f64)
     xe = np.asarray(xe, dtype=f64)
@@ -450,7 +478,7 @@ def sampled_token_outputs(x, logits, W1, W2, dout, k, tokens, mx=False):
         # Row-local backward: dY1 row quantisation and the dgrads need only
         # the row itself; the wgrad outputs of expert_backward are discarded.
         dy2 = dout[tokens[ti]].astype(f64)
-        g, u = s["g"], s["u"]
+        g, u = saved_gate_up(s["g"], s["u"], mx)
         dy2_row = mx_qdq(dy2, axis=1) if mx else dy2
         dh = dy2_row @ _w2_dgrad(W2[e], mx).T
         a = silu(g) * u
@@ -501,8 +529,8 @@ def sampled_weight_grads(x, logits, W1, W2, dout, k, fcols, mx=False):
             W1e[:, np.concatenate([fcols, F + fcols])]
         y1 = xin @ W1f
         g, u = y1[:, :nc], y1[:, nc:]
-        a = silu(g) * u
-        h = a * p
+        h = silu(g) * u * p
+        g, u = saved_gate_up(g, u, mx)
         # dH columns c: dY2 (row-quantised along H) times W2 rows c (quantised along H).
         dy2 = dout[tok].astype(f64)
         dy2_row = mx_qdq(dy2, axis=1) if mx else dy2

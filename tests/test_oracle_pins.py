@@ -187,6 +187,24 @@ def test_e4m3_round_matches_library_conversion():
     np.testing.assert_array_equal(ours, lib)
 
 
+def test_bf16_round_matches_library_conversion():
+    # torch's float32 -> bfloat16 cast rounds to nearest even; the oracle's
+    # bit-level rounding does not call it, so agreement pins to_bf16.
+    rng = np.random.default_rng(12)
+    v = np.concatenate([
+        rng.standard_normal(100000) * np.exp2(rng.uniform(-60, 60, 100000)),
+        # exact midpoints between neighbouring bf16 values, both parities
+        (np.arange(1, 20001, dtype=np.uint32) << 16 | 0x8000).view(np.float32),
+        -(np.arange(1, 20001, dtype=np.uint32) << 16 | 0x8000).view(np.float32),
+        [0.0, -0.0, np.inf, -np.inf, 3.3895313892515355e38, 1e-45, -1e-40],
+    ]).astype(np.float32)
+    ours = O.to_bf16(v)
+    lib = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(ours, lib)
+    assert np.signbit(O.to_bf16(np.array([-0.0])))[0]
+    assert np.isnan(O.to_bf16(np.array([np.nan])))[0]
+
+
 def test_mxfp8_roundtrip_exact_on_representable_blocks():
     rng = np.random.default_rng(5)
     grid = O.e4m3_decode(np.arange(0, 127))  # non-negative finite grid
