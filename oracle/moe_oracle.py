@@ -206,6 +206,36 @@ def e8m0_decode(s):
     return np.where(s == 255, np.nan, np.ldexp(1.0, s - 127))
 
 
+def _blocks(a, axis):
+    """View of ``a`` as [outer, n/32, 32, inner]: the 32-blocks along ``axis``."""
+    a = np.asarray(a, dtype=f64)
+    axis = axis % a.ndim
+    n = a.shape[axis]
+    if n % MX_BLOCK:
+        raise ValueError("blocked axis must be a multiple of 32")
+    outer = int(np.prod(a.shape[:axis], dtype=np.int64))
+    inner = int(np.prod(a.shape[axis + 1:], dtype=np.int64))
+    return a.reshape(outer, n // MX_BLOCK, MX_BLOCK, inner)
+
+
+def _block_exponent(blk):
+    """Per block: whether it is finite, and the shared scale exponent
+    e = clamp(floor(log2 amax) - 8, -127, 127), -127 for an all-zero block."""
+    amax = np.abs(blk).max(axis=2)  # NaN propagates; Inf stays Inf
+    finite = np.isfinite(amax)
+    _, ex = np.frexp(np.where(finite, amax, 0.0))  # amax = m * 2^ex, m in [0.5, 1)
+    e = np.where(finite & (amax > 0), ex - 1 - E4M3_EMAX, -127)
+    return finite, np.clip(e, -127, 127)
+
+
+def _scaled_magnitudes(blk, finite, e):
+    """RNE_E4M3(|v| * 2^-e) of every element (0 inside non-finite blocks)."""
+    scaled = np.abs(blk) * np.ldexp(1.0, -e)[:, :, None, :]  # exact: a power of two
+    if not finite.all():
+        scaled = np.where(finite[:, :, None, :], scaled, 0.0)
+    return e4m3_round(scaled)
+
+
 def mx_quantize(a, axis=-1):
     """MXFP8 (E4M3 elements, E8M0 scales) with 32-blocks along ``axis``.
 
@@ -214,24 +244,16 @@ def mx_quantize(a, axis=-1):
     element = RNE_E4M3(v * 2^-e), saturated to +-448.
     Returns (codes uint8 shaped like a, scales uint8 with the axis divided by 32).
     """
-    a = np.moveaxis(np.asarray(a, dtype=f64), axis, -1)
-    n = a.shape[-1]
-    if n % MX_BLOCK:
-        raise ValueError("blocked axis must be a multiple of 32")
-    blk = a.reshape(a.shape[:-1] + (n // MX_BLOCK, MX_BLOCK))
-    finite = np.isfinite(blk).all(axis=-1)
-    amax = np.where(finite, np.abs(np.where(np.isfinite(blk), blk, 0)).max(axis=-1), 0.0)
-    _, ex = np.frexp(amax)
-    e = np.where(amax > 0, ex - 1 - E4M3_EMAX, -127)
-    e = np.clip(e, -127, 127)
-    scaled = blk * np.ldexp(1.0, -e)[..., None]
-    mag = e4m3_round(np.abs(np.where(np.isfinite(scaled), scaled, 0)))
+    shape = np.shape(a)
+    axis = axis % len(shape)
+    blk = _blocks(a, axis)
+    finite, e = _block_exponent(blk)
+    mag = _scaled_magnitudes(blk, finite, e)
     codes = e4m3_encode(np.signbit(blk), mag)
-    codes = np.where(finite[..., None], codes, np.uint8(0x7F)).astype(np.uint8)
+    codes = np.where(finite[:, :, None, :], codes, np.uint8(0x7F)).astype(np.uint8)
     scales = np.where(finite, e + 127, 255).astype(np.uint8)
-    codes = np.moveaxis(codes.reshape(a.shape), -1, axis)
-    scales = np.moveaxis(scales, -1, axis)
-    return codes, scales
+    sshape = shape[:axis] + (shape[axis] // MX_BLOCK,) + shape[axis + 1:]
+    return codes.reshape(shape), scales.reshape(sshape)
 
 
 def mx_dequantize(codes, scales, axis=-1):
@@ -242,10 +264,30 @@ def mx_dequantize(codes, scales, axis=-1):
     return np.moveaxis(v.reshape(c.shape), -1, axis)
 
 
+MX_SLAB = 1 << 21  # elements per slab of blocks handled at once by mx_qdq
+
+
 def mx_qdq(a, axis=-1):
-    """Quantise then dequantise: the values an MXFP8 GEMM operand carries."""
-    c, s = mx_quantize(a, axis)
-    return mx_dequantize(c, s, axis)
+    """The values an MXFP8 GEMM operand carries: each element's quantised
+    value times its block's scale, sign(v) * RNE_E4M3(|v| * 2^-e) * 2^e
+    (NaN in a block holding Inf or NaN). This is mx_dequantize(mx_quantize(a))
+    without the round trip through the byte encoding. Blocks are independent,
+    so they are handled a slab of about MX_SLAB elements at a time, which
+    bounds the temporary memory of very large operands."""
+    b4 = _blocks(a, axis)
+    inner = b4.shape[3]
+    blk = b4.reshape(-1, 1, MX_BLOCK, inner)  # one row per 32-block (times inner)
+    out = np.empty(blk.shape)
+    step = max(1, MX_SLAB // (MX_BLOCK * inner))
+    for i in range(0, blk.shape[0], step):
+        b = blk[i:i + step]
+        finite, e = _block_exponent(b)
+        v = _scaled_magnitudes(b, finite, e) * np.ldexp(1.0, e)[:, :, None, :]
+        v = np.copysign(v, b)
+        if not finite.all():
+            v = np.where(finite[:, :, None, :], v, np.nan)
+        out[i:i + step] = v
+    return out.reshape(np.shape(a))
 
 
 def mx_qdq_cols_in_groups(a):
@@ -451,6 +493,20 @@ def layer_fwd_bwd_expert_stream(x, logits, W1, W2, dout, k, mx=False):
 # Sampled mode: exact values at chosen positions of very large layers
 # ---------------------------------------------------------------------------
 
+SAMPLED_THREADS = 4
+
+
+def map_experts(fn, E):
+    """[fn(e) for e in range(E)]. Experts share no state, so a few host
+    threads run them at once (numpy releases the interpreter lock inside its
+    array operations); every expert's arithmetic is unchanged."""
+    from concurrent.futures import ThreadPoolExecutor
+    workers = max(1, min(E, SAMPLED_THREADS))
+    if workers == 1:
+        return [fn(e) for e in range(E)]
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        return list(ex.map(fn, range(E)))
+
 def sampled_token_outputs(x, logits, W1, W2, dout, k, tokens, mx=False):
     """out, dX and dlogits for the given tokens only.
 
@@ -468,10 +524,11 @@ def sampled_token_outputs(x, logits, W1, W2, dout, k, tokens, mx=False):
     out = np.zeros((nt, H))
     dX = np.zeros((nt, H))
     dp = np.zeros((nt, k))
-    for e in range(E):
+
+    def one(e):
         ti, sj = expert_rows(idx_all, e)
         if ti.size == 0:
-            continue
+            return None
         xe = x[tokens[ti]].astype(f64)
         p = w_all[ti, sj]
         y2, s = expert_forward(xe, p, W1[e], W2[e], mx)
@@ -487,6 +544,12 @@ def sampled_token_outputs(x, logits, W1, W2, dout, k, tokens, mx=False):
         dy1 = np.concatenate([dA * u * dsilu(g), dA * silu(g)], axis=1)
         dy1_row = mx_qdq(to_f32(dy1), axis=1) if mx else dy1
         dxp = dy1_row @ _w1_dgrad(W1[e], mx).T
+        return ti, sj, y2, dxp, dpe
+
+    for r in map_experts(one, E):  # combined in expert order
+        if r is None:
+            continue
+        ti, sj, y2, dxp, dpe = r
         np.add.at(out, ti, y2)
         np.add.at(dX, ti, dxp)
         dp[ti, sj] = dpe
@@ -515,10 +578,11 @@ def sampled_weight_grads(x, logits, W1, W2, dout, k, fcols, mx=False):
     dW1g = np.zeros((E, H, nc))
     dW1u = np.zeros((E, H, nc))
     dW2s = np.zeros((E, nc, H))
-    for e in range(E):
+
+    def one(e):
         tok, slot = expert_rows(idx, e)
         if tok.size == 0:
-            continue
+            return
         xe = x[tok].astype(f64)
         p = w[tok, slot][:, None]
         W1e = np.asarray(W1[e], dtype=f64)
@@ -550,6 +614,8 @@ def sampled_weight_grads(x, logits, W1, W2, dout, k, fcols, mx=False):
         dW2s[e] = h_col.T @ dy2_col
         dW1g[e] = x_col.T @ dg_col
         dW1u[e] = x_col.T @ du_col
+
+    map_experts(one, E)
     return {"dW1g": dW1g, "dW1u": dW1u, "dW2": dW2s}
 
 

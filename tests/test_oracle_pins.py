@@ -205,6 +205,27 @@ def test_bf16_round_matches_library_conversion():
     assert np.isnan(O.to_bf16(np.array([np.nan])))[0]
 
 
+@pytest.mark.parametrize("axis", [0, 1, 2])
+def test_mx_qdq_equals_decoded_codes(axis):
+    # mx_qdq skips the byte encoding; it must equal decoding the codes and
+    # scales that mx_quantize writes (the decode is pinned by the library
+    # E4M3 table above), on random and special blocks.
+    rng = np.random.default_rng(13)
+    a = rng.standard_normal((64, 96, 64)) * np.exp2(rng.integers(-140, 140, (64, 1, 1)))
+    a[0, :32] = 0.0
+    a[1, :32] = -0.0
+    a[2, 5] = 1e4  # saturating
+    a[3, 7] = np.inf
+    a[4, 9, 3] = np.nan
+    codes, scales = O.mx_quantize(a, axis=axis)
+    ref = O.mx_dequantize(codes, scales, axis=axis)
+    got = O.mx_qdq(a, axis=axis)
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[ok], ref[ok])
+    np.testing.assert_array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+
+
 def test_mxfp8_roundtrip_exact_on_representable_blocks():
     rng = np.random.default_rng(5)
     grid = O.e4m3_decode(np.arange(0, 127))  # non-negative finite grid
