@@ -158,6 +158,8 @@ MOE_API int moe_permute_plan_static(const int32_t* idx, int T, int E, int k, int
  *   w, p_rows: optional (both NULL or both set): p_rows[dest[i]] = w[i]
  *   (fp32 [R_pad], 0 on padding rows), the per-row routing weight used by
  *   the scaled-SwiGLU epilogue.
+ *   xp may be NULL when p_rows is set: then only p_rows is written (the
+ *   MXFP8 path gathers x inside mxfp8_quantize instead) and x is not read.
  * Requires H % 8 == 0 and 16-byte aligned x and xp. */
 MOE_API int moe_permute(const void* x, const int32_t* dest, const int32_t* offsets,
                 const int32_t* counts, const float* w, int T, int H, int E, int k, void* xp,
@@ -309,7 +311,8 @@ MOE_API int moe_fc1_swiglu_mxfp8(const uint8_t* xq, const uint8_t* sx, long long
  *   dH = dy2 * W2_e^T; with g, u from gu and p = p_rows[r]:
  *   dY1 = [dA*u*silu'(g) | dA*silu(g)] (dA = dH*p) written as row-wise MXFP8
  *   dy1q_row [rows, 2F] + sdy1_row and column-wise dy1q_col [2F, rows] +
- *   sdy1_col; dp_part[r, c] (c < ceil(F/256)) partial sums of dH*silu(g)*u.
+ *   sdy1_col; dp_part [rows, 2*ceil(F/256)] fp32: partial sums of
+ *   dH*silu(g)*u (their sum over c is dL/dp of the row).
  * Requires rows, H, F multiples of 128. */
 MOE_API int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t* sdy2,
                                            long long rows, int H, const uint8_t* w2q,
@@ -333,12 +336,27 @@ MOE_API int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t* s
  *   dx [T, H] bf16, dw1 [E, H, 2F] bf16, dw2 [E, F, H] bf16,
  *   dlogits [T, E] fp32 (through the top-k softmax weights only).
  *   Must follow moe_layer_forward with the same cfg, weights and workspace.
- * Requirements: H % 128 == 0, F % 128 == 0, 1 <= k <= 8, k <= E <= 256,
- * align a multiple of 128 (groups are padded with zero rows), precision
- * MOE_PRECISION_BF16. moe_layer_workspace_size returns 0 for an unsupported
- * cfg. The workspace must be 256-byte aligned.
+ * Precision:
+ *   MOE_PRECISION_BF16: bf16 operands, fp32 accumulation; [g|u], H and the
+ *     permuted activations are kept in bf16.
+ *   MOE_PRECISION_MXFP8 (§Challenge 2 and 3): x, W1, W2 and dOut are
+ *     quantised to MXFP8 (the permutes of x and dOut are fused into their
+ *     quantisation; both weights are quantised once per forward, row- and
+ *     column-wise); the FC1 epilogue emits H and the FC2-dgrad epilogue emits
+ *     dY1 as MXFP8 in both directions; every GEMM takes operands whose
+ *     32-blocks run along its reduction dimension (row-wise for forward and
+ *     dgrad, column-wise within an expert group for wgrad). [g|u] is kept in
+ *     bf16 for the SwiGLU backward.
+ * Requirements: H % 128 == 0 (H % 256 == 0 for MXFP8), F % 128 == 0,
+ * 1 <= k <= 8, k <= E <= 256, align a multiple of 128 (groups are padded with
+ * zero rows). moe_layer_workspace_size returns 0 for an unsupported cfg. The
+ * workspace must be 256-byte aligned.
  * moe_layer_workspace_part gives the byte offset and size of one saved
- * intermediate (MOE_PART_*) inside the workspace, for inspection.
+ * intermediate (MOE_PART_*) inside the workspace, for inspection; parts of
+ * the other precision have size 0. R_max = T*k + E*(align-1), rounded up to
+ * a multiple of 128 in MXFP8 mode. MXFP8 parts come in fours: data of the
+ * row-wise copy [rows, cols], its tiled scales, data of the column-wise copy
+ * [cols, rows] and its tiled scales (layouts as in mxfp8_quantize).
  */
 #define MOE_PRECISION_BF16 0
 #define MOE_PRECISION_MXFP8 1
@@ -354,9 +372,22 @@ typedef struct moe_layer_config {
 #define MOE_PART_OFFSETS 3  /* int32 [E + 1] */
 #define MOE_PART_DEST 4     /* int32 [T * k] */
 #define MOE_PART_SRC 5      /* int32 [R_max] */
+#define MOE_PART_PROWS 7    /* fp32 [R_max]: routing weight of each permuted row */
 #define MOE_PART_XP 8       /* bf16 [R_max, H] */
 #define MOE_PART_GU 9       /* bf16 [R_max, 2F] */
 #define MOE_PART_H 10       /* bf16 [R_max, F] */
+#define MOE_PART_Y2 11      /* bf16 [R_max, H]: FC2 output */
+#define MOE_PART_DY2 12     /* bf16 [R_max, H]: dOut gathered (BF16 mode) */
+#define MOE_PART_DY1 13     /* bf16 [R_max, 2F]: [dg | du] (BF16 mode) */
+#define MOE_PART_DXP 14     /* bf16 [R_max, H]: FC1 dgrad output */
+#define MOE_PART_DP 15      /* fp32 [R_max, n_part]: partial sums of dL/dw per row */
+#define MOE_PART_XQ_ROW 16  /* MXFP8 x gathered: [R_max, H] (+ 17, 18, 19) */
+#define MOE_PART_W1Q_ROW 20 /* MXFP8 W1 viewed [E*H, 2F] (+ 21, 22, 23) */
+#define MOE_PART_W2Q_ROW 24 /* MXFP8 W2 viewed [E*F, H] (+ 25, 26, 27) */
+#define MOE_PART_HQ_ROW 28  /* MXFP8 H: [R_max, F] (+ 29, 30, 31) */
+#define MOE_PART_DY2Q_ROW 32 /* MXFP8 dOut gathered: [R_max, H] (+ 33, 34, 35) */
+#define MOE_PART_DY1Q_ROW 36 /* MXFP8 dY1: [R_max, 2F] (+ 37, 38, 39) */
+#define MOE_PART_DY1S_COL 39
 
 MOE_API size_t moe_layer_workspace_size(const moe_layer_config* cfg);
 MOE_API int moe_layer_workspace_part(const moe_layer_config* cfg, int part, size_t* offset,

@@ -324,7 +324,7 @@ def moe_fc2_dgrad_swiglu_bwd_mxfp8(dy2q, sdy2, w2q, sw2, offsets, p_rows, gu, F,
                "s_row": torch.empty(mx_scale_bytes(rows, 2 * F), dtype=torch.uint8, device=dev),
                "q_col": torch.empty((2 * F, rows), dtype=torch.uint8, device=dev),
                "s_col": torch.empty(mx_scale_bytes(2 * F, rows), dtype=torch.uint8, device=dev),
-               "dp": torch.empty((rows, -(-F // 256)), dtype=torch.float32, device=dev)}
+               "dp": torch.empty((rows, 2 * -(-F // 256)), dtype=torch.float32, device=dev)}
     _check(lib().moe_fc2_dgrad_swiglu_bwd_mxfp8(ptr(dy2q), ptr(sdy2), rows, H, ptr(w2q), ptr(sw2),
                                                 ptr(offsets), ptr(p_rows), ptr(gu), E, F,
                                                 ptr(out["q_row"]), ptr(out["s_row"]),
@@ -339,7 +339,13 @@ def moe_fc2_dgrad_swiglu_bwd_mxfp8(dy2q, sdy2, w2q, sw2, offsets, p_rows, gu, F,
 PRECISION = {"bf16": 0, "mxfp8": 1}
 PARTS = {"idx": (0, torch.int32), "w": (1, torch.float32), "counts": (2, torch.int32),
          "offsets": (3, torch.int32), "dest": (4, torch.int32), "src": (5, torch.int32),
-         "xp": (8, torch.bfloat16), "gu": (9, torch.bfloat16), "h": (10, torch.bfloat16)}
+         "p_rows": (7, torch.float32), "xp": (8, torch.bfloat16), "gu": (9, torch.bfloat16),
+         "h": (10, torch.bfloat16), "y2": (11, torch.bfloat16), "dy2": (12, torch.bfloat16),
+         "dy1": (13, torch.bfloat16), "dxp": (14, torch.bfloat16), "dp": (15, torch.float32)}
+# MXFP8 parts: four per operand (row-wise data, its scales, column-wise data, its scales)
+for _i, _name in enumerate(("x", "w1", "w2", "h", "dy2", "dy1")):
+    for _j, _suffix in enumerate(("q_row", "s_row", "q_col", "s_col")):
+        PARTS[f"{_name}_{_suffix}"] = (16 + 4 * _i + _j, torch.uint8)
 
 
 class LayerConfig(C.Structure):

@@ -174,7 +174,14 @@ __device__ __forceinline__ void load32_bf16(const __nv_bfloat16* src, float* v) 
   }
 }
 
-__device__ __forceinline__ float sigmoidf_fast(float z) { return 1.f / (1.f + __expf(-z)); }
+// Logistic function from the hardware exponential and the hardware
+// approximate reciprocal (relative error ~2^-22; 1/inf = 0 gives 0 for very
+// negative z).
+__device__ __forceinline__ float sigmoidf_fast(float z) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + __expf(-z)));
+  return r;
+}
 
 template <int MODE, int EPI, int BN, int A_MN, int B_MN>
 __global__ void __launch_bounds__(kThreads, 1)

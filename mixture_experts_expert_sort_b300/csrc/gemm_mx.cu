@@ -16,12 +16,17 @@
 //    memory with tcgen05.cp (32x128b, replicated to the four lane quarters)
 //    and issues four K=32 MMAs; scale byte kb of each 32-bit TMEM word is
 //    selected by the instruction descriptor's scale ids.
-//  * Tensor memory: the two fp32 accumulators (N = 256 columns each) would
-//    fill all 512 columns and leave none for scales. Instead tiles alternate
-//    between columns [0, 256) and [128, 384); the epilogue drains the shared
-//    region [128, 256) first and releases it, so the next tile's MMAs start
-//    while the epilogue still works on the other half. Columns [384, 512)
-//    hold the scale factors of the shared-memory stages.
+//  * Tensor memory: two full fp32 accumulators (N = 256 columns each) would
+//    fill all 512 columns and leave none for scales. Tiles alternate between
+//    columns [0, 256) and [192, 448), which share [192, 256). The epilogue
+//    first copies the shared 64 columns to registers and releases them, so
+//    the next tile's MMAs start while the epilogue still works on the rest.
+//    Columns [448, 512) hold the scale factors of the shared-memory stages.
+//  * Quantising epilogues: each warp owns 32 rows of the tile, one per lane.
+//    Row-wise blocks (32 columns of one row) are quantised by their lane.
+//    Column-wise blocks (one column over the warp's 32 rows) are transposed
+//    through a per-warp shared-memory buffer, after which each lane holds one
+//    column and quantises it like a row, storing its 32 contiguous bytes.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -37,30 +42,55 @@ using gemm::EPI_SWIGLU_BWD;
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 128;  // bytes of E4M3 = elements per stage
-constexpr int kStages = 4;
-constexpr int kThreads = 192;
 constexpr int kMaxGroups = gemm::kMaxGroups;
 
 constexpr int kABytes = BM * BK;
 constexpr int kBBytes = BN * BK;
 constexpr int kSfaBytes = 512;
 constexpr int kSfbBytes = 1024;
-// A/B stages stay 1024-byte aligned (128B-swizzle atoms); the scale tiles of
-// all stages follow in a region of their own.
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kSfStageBytes = kSfaBytes + kSfbBytes;
 constexpr int kTxBytes = kStageBytes + kSfStageBytes;
-constexpr int kSfOffset = kStages * kStageBytes;
-constexpr int kBarOffset = kSfOffset + kStages * kSfStageBytes;
-// full[S], empty[S], tfull[2], region_empty[3], drain
-constexpr int kNumBars = 2 * kStages + 6;
-constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
-constexpr int kPrefixOffset = kMiscOffset + 16;
-constexpr int kSmemBytes = kPrefixOffset + (kMaxGroups + 1) * 4;
-constexpr int kSmemAlloc = kSmemBytes + 1024;
-constexpr int kSfTmemCol = 384;  // scale factors live in TMEM columns [384, 512)
+// Per-warp transpose buffer of the column-wise quantiser: 32 rows x 36 words
+// (rows 16-byte aligned for vector writes; column reads hit 32 banks).
+constexpr int kXposeStride = 36;
+constexpr int kXposeWords = 32 * kXposeStride;
+constexpr int kGuRowBytes = 144;
+
+// Shared-memory layout and warp counts of one kernel flavour. The plain
+// (store / wgrad) kernels use a 4-stage ring and 4 epilogue warps; the fused
+// quantising epilogues carry much more work per tile, so they run 8
+// epilogue warps (two per TMEM lane quarter, each taking every other
+// 32-column chunk) and keep a 3-stage ring to make room for the warps'
+// transpose buffers.
+template <bool FUSED>
+struct Cfg {
+  static constexpr int kStages = FUSED ? 3 : 4;
+  static constexpr int kEpiWarps = FUSED ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  // A/B stages stay 1024-byte aligned (128B-swizzle atoms); the scale tiles
+  // of all stages follow in a region of their own.
+  static constexpr int kSfOffset = kStages * kStageBytes;
+  static constexpr int kXposeOffset = kSfOffset + kStages * kSfStageBytes;
+  // Per-warp staging of the saved gate/up values the backward epilogue reads
+  // (cp.async): 32 rows x (64 B gate + 64 B up), rows padded to 144 B.
+  static constexpr int kGuOffset = kXposeOffset + (FUSED ? kEpiWarps * kXposeWords * 4 : 0);
+  static constexpr int kBarOffset = kGuOffset + (FUSED ? kEpiWarps * 32 * kGuRowBytes : 0);
+  // full[S], empty[S], tfull[2], region_empty[3], drain
+  static constexpr int kNumBars = 2 * kStages + 6;
+  static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
+  static constexpr int kPrefixOffset = kMiscOffset + 16;
+  static constexpr int kSmemBytes = kPrefixOffset + (kMaxGroups + 1) * 4;
+  static constexpr int kSmemAlloc = kSmemBytes + 1024;
+  static_assert(kSmemAlloc <= 232448, "shared memory budget");
+};
+
+// Tensor-memory columns.
+constexpr int kAcc1Col = 192;     // accumulator of odd tiles: [192, 448)
+constexpr int kSfTmemCol = 448;   // scale factors: [448, 512)
 constexpr int kSfColsPerStage = 12;  // 4 (A) + 8 (B)
-static_assert(kSfTmemCol + kStages * kSfColsPerStage <= 512, "TMEM budget");
+static_assert(kSfTmemCol + 4 * kSfColsPerStage <= 512, "TMEM budget");
+static_assert(kAcc1Col + BN <= kSfTmemCol, "TMEM budget");
 
 struct MxParams {
   const int32_t* offsets;
@@ -132,15 +162,11 @@ __device__ __forceinline__ int b_half_row(const MxParams& p, int nt, int h) {
 // Row-wise MXFP8 of 32 consecutive values held by one thread: 32 code bytes
 // to dst (16-byte aligned) and the scale byte to *sdst.
 __device__ __forceinline__ void quant_row32(const float* v, uint8_t* dst, uint8_t* sdst) {
-  float amax = 0.f;
-  bool finite = true;
+  // Non-negative floats order like their bit patterns; Inf and NaN are the largest.
+  uint32_t mbits = 0;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    float a = fabsf(v[i]);
-    finite = finite && (a <= 3.402823466e38f);
-    amax = fmaxf(amax, a);
-  }
-  const uint32_t sb = finite ? mx_scale_byte(amax) : 0xFFu;
+  for (int i = 0; i < 32; ++i) mbits = max(mbits, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+  const uint32_t sb = mbits < 0x7F800000u ? mx_scale_byte(__uint_as_float(mbits)) : 0xFFu;
   uint32_t w[8];
   if (sb == 0xFFu) {
 #pragma unroll
@@ -158,25 +184,205 @@ __device__ __forceinline__ void quant_row32(const float* v, uint8_t* dst, uint8_
   *sdst = (uint8_t)sb;
 }
 
-// Column-wise MXFP8 of one value per lane (the 32 lanes of the warp hold 32
-// consecutive rows of one column): the warp agrees on the block's scale and
-// each lane returns its code byte; the scale byte is returned to every lane.
-__device__ __forceinline__ uint32_t quant_col_lane(float v, uint32_t& sb_out) {
-  const float a = fabsf(v);
-  // Non-negative floats order like their bit patterns; Inf/NaN bits are the largest.
-  const uint32_t bits = __float_as_uint(a);
-  const uint32_t mbits = __reduce_max_sync(0xffffffffu, bits);
-  const bool finite = mbits < 0x7F800000u;
-  const uint32_t sb = finite ? mx_scale_byte(__uint_as_float(mbits)) : 0xFFu;
-  sb_out = sb;
-  if (sb == 0xFFu) return 0x7Fu;
-  return (uint32_t)cvt_e4m3x2(v * mx_inv_scale(sb), 0.f) & 0xFFu;
+// Column-wise MXFP8 of a 32 x 32 block held one row per lane (v[i] is row
+// `lane`, column i): every column is one block. The block is transposed
+// through this warp's buffer `xs` (32 rows of kXposeStride words), after
+// which lane c holds column c and quantises it like a row: its 32 codes go to
+// q + (f0 + c) * ld + rb and its scale byte to the tiled layout of an operand
+// with ld columns. Called by all 32 lanes of the warp.
+__device__ __forceinline__ void quant_col_block32(const float* v, uint8_t* q, uint8_t* sq,
+                                                  long long ld, long long f0, long long rb,
+                                                  float* xs, int lane) {
+  __syncwarp();
+  float4* row = reinterpret_cast<float4*>(xs + lane * kXposeStride);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) row[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  __syncwarp();
+  float c[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) c[r] = xs[r * kXposeStride + lane];
+  quant_row32(c, q + (f0 + lane) * ld + rb, sq + mx_scale_offset(f0 + lane, rb >> 5, ld));
+}
+
+// Tile-local accumulator chunk c (32 columns) of this warp's 32 rows: from
+// the registers sh when the chunk lies in the shared TMEM region (already
+// drained: local chunks 6, 7 of even tiles, 0, 1 of odd tiles), else from
+// TMEM. NSH = 2: the warp drained both shared chunks (sh[0..63]); NSH = 1:
+// it takes only chunks of parity h and drained the one of them that is
+// shared (sh[0..31]). c is a run-time value; sh is read at constant indices.
+template <int NSH>
+__device__ __forceinline__ void acc_chunk(int c, bool odd, int h, const float* sh,
+                                          uint32_t tl_tile, float* f) {
+  const int s = odd ? c : c - 6;
+  if (NSH == 2 ? s == 0 : s == h) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] = sh[i];
+  } else if (NSH == 2 && s == 1) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] = sh[NSH == 2 ? 32 + i : i];
+  } else {
+    uint32_t v[32];
+    ptx::tmem_ld_32x32b_x32(tl_tile + c * 32, v);
+    ptx::tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+  }
+}
+
+// Asynchronous copy of this lane's row of a 32-column gate/up chunk
+// (2 x 64 bytes of bf16) into its staging row in shared memory.
+__device__ __forceinline__ void stage_gu_chunk(const MxParams& p, long long grow, long long col,
+                                               uint32_t dst) {
+  const __nv_bfloat16* g = p.GU + grow * 2 * p.F + col;
+  const __nv_bfloat16* u = g + p.F;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    ptx::cp_async_16(dst + 16 * i, g + 8 * i);
+    ptx::cp_async_16(dst + 64 + 16 * i, u + 8 * i);
+  }
+  ptx::cp_async_commit();
+}
+
+// Element i (a compile-time index after unrolling) of 32 packed bf16 values.
+__device__ __forceinline__ float bf16_at(const uint4* s, int i) {
+  const uint4 v = s[i >> 3];
+  const int w = (i >> 1) & 3;
+  const uint32_t word = w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+  return (i & 1) ? gemm::bf16_hi(word) : gemm::bf16_lo(word);
+}
+
+__device__ __forceinline__ void unpack_bf16x32(const uint4* s, float* v) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t w[4] = {s[q].x, s[q].y, s[q].z, s[q].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * q + 2 * j] = gemm::bf16_lo(w[j]);
+      v[8 * q + 2 * j + 1] = gemm::bf16_hi(w[j]);
+    }
+  }
+}
+
+// The epilogue of one tile for this warp's 32 rows (lane = row). Fused
+// epilogues split the tile's 32-column chunks between two warps per lane
+// quarter by parity h; the plain ones take every chunk (h = 0, NSH = 2).
+template <int MODE, int EPI>
+__device__ __forceinline__ void epilogue_tile(const MxParams& p, const TileInfo& ti, bool odd,
+                                              int h, const float* sh, uint32_t tl_tile, int q,
+                                              int lane, float* xs, uint8_t* gu_stage) {
+  const long long lrow = (long long)ti.mt * BM + q * 32 + lane;
+  const bool has_acc = ti.k_iters > 0;
+  if (MODE == WGRAD) {
+    __nv_bfloat16* crow = p.C + (long long)ti.e * p.c_group_stride + lrow * p.ldc +
+                          (long long)ti.nt * BN;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      float f[32];
+      if (has_acc) {
+        acc_chunk<2>(c, odd, 0, sh, tl_tile, f);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) f[i] = 0.f;
+      }
+      gemm::store32_bf16(crow + c * 32, f);
+    }
+    return;
+  }
+  const bool row_ok = lrow < ti.rows;
+  const long long grow = ti.row0 + lrow;
+  const long long rb = ti.row0 + (long long)ti.mt * BM + q * 32;  // first row of the warp
+  if (EPI == EPI_STORE) {
+    const int ncol = p.N - ti.nt * BN;
+    __nv_bfloat16* crow = p.C + grow * p.ldc + (long long)ti.nt * BN;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      float f[32];
+      acc_chunk<2>(c, odd, 0, sh, tl_tile, f);
+      if (row_ok && c * 32 < ncol) gemm::store32_bf16(crow + c * 32, f);
+    }
+  } else if (EPI == EPI_SWIGLU_FWD) {
+    // Tile-local chunks 0..3 are gate, 4..7 are up, for F-columns n0 .. n0+127;
+    // this warp takes h-columns chunks c = h, h + 2.
+    const float pr = row_ok ? p.p_rows[grow] : 0.f;
+    const long long F = p.F;
+#pragma unroll 1
+    for (int c = h; c < 4; c += 2) {
+      float g[32], u[32];
+      acc_chunk<1>(c, odd, h, sh, tl_tile, g);
+      acc_chunk<1>(c + 4, odd, h, sh, tl_tile, u);
+      const long long col = (long long)ti.nt * (BN / 2) + c * 32;
+      if (row_ok) {
+        gemm::store32_bf16(p.GU + grow * 2 * F + col, g);
+        gemm::store32_bf16(p.GU + grow * 2 * F + F + col, u);
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) g[i] = g[i] * gemm::sigmoidf_fast(g[i]) * u[i] * pr;  // h
+      if (row_ok)
+        quant_row32(g, p.q_row + grow * p.q_row_ld + col,
+                    p.s_row + mx_scale_offset(grow, col >> 5, p.q_row_ld));
+      quant_col_block32(g, p.q_col, p.s_col, p.q_col_ld, col, rb, xs, lane);
+    }
+  } else {  // EPI_SWIGLU_BWD: accumulator = dH for F-columns nt*256 + [0, 256)
+    const float pr = row_ok ? p.p_rows[grow] : 0.f;
+    const long long F = p.F;
+    const int ncol = p.N - ti.nt * BN;
+    float dp = 0.f;
+    // Saved gate/up of this warp's next chunk, staged into shared memory
+    // while the current chunk is quantised (rows are whole 128-row groups,
+    // so every lane's row is valid).
+    const uint32_t gu_row = ptx::smem_u32(gu_stage) + lane * kGuRowBytes;
+    const uint4* gu_mine = reinterpret_cast<const uint4*>(gu_stage + lane * kGuRowBytes);
+    if (h * 32 < ncol) stage_gu_chunk(p, grow, (long long)ti.nt * BN + h * 32, gu_row);
+#pragma unroll 1
+    for (int c = h; c < 8 && c * 32 < ncol; c += 2) {  // N tail: uniform across the warp
+      const long long col = (long long)ti.nt * BN + c * 32;
+      float dg[32], du[32];
+      acc_chunk<1>(c, odd, h, sh, tl_tile, dg);  // dH for now
+      ptx::cp_async_wait_all();
+      uint4 gc[4], uc[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        gc[i] = gu_mine[i];
+        uc[i] = gu_mine[4 + i];
+      }
+      if (c + 2 < 8 && (c + 2) * 32 < ncol) stage_gu_chunk(p, grow, col + 64, gu_row);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float g = bf16_at(gc, i), u = bf16_at(uc, i);
+        const float sg = gemm::sigmoidf_fast(g);
+        const float silu = g * sg;
+        dp = fmaf(dg[i], silu * u, dp);
+        const float da = dg[i] * pr;  // dA = dH * p
+        dg[i] = da * u * sg * (1.f + g * (1.f - sg));
+        du[i] = da * silu;
+      }
+      // dg into columns [0, F), du into [F, 2F), both directions.
+      if (row_ok) {
+        quant_row32(dg, p.q_row + grow * p.q_row_ld + col,
+                    p.s_row + mx_scale_offset(grow, col >> 5, p.q_row_ld));
+        quant_row32(du, p.q_row + grow * p.q_row_ld + F + col,
+                    p.s_row + mx_scale_offset(grow, (F + col) >> 5, p.q_row_ld));
+      }
+      quant_col_block32(dg, p.q_col, p.s_col, p.q_col_ld, col, rb, xs, lane);
+      quant_col_block32(du, p.q_col, p.s_col, p.q_col_ld, F + col, rb, xs, lane);
+    }
+    // This warp's partial of dL/dp over its chunks; the two warps of a lane
+    // quarter write the two halves of the tile's partial (n_part = 2 per tile).
+    if (row_ok) p.dp_part[grow * p.n_part + 2 * ti.nt + h] = dp;
+  }
 }
 
 template <int MODE, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
     grouped_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB, const MxParams p) {
+  using L = Cfg<EPI != EPI_STORE>;
+  constexpr int kStages = L::kStages;
+  constexpr int kSfOffset = L::kSfOffset;
+  constexpr int kBarOffset = L::kBarOffset;
+  constexpr int kMiscOffset = L::kMiscOffset;
+  constexpr int kPrefixOffset = L::kPrefixOffset;
+  constexpr int kEpiThreads = 32 * L::kEpiWarps;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -185,6 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+  // TMEM regions: 0 = [0, 192) (even tiles only), 1 = [192, 256) (shared),
+  // 2 = [256, 448) (odd tiles only).
   auto region_bar = [&](int r) { return bar0 + 8u * (2 * kStages + 2 + r); };
   const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 5);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kMiscOffset);
@@ -200,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) ptx::mbar_init(tfull_bar(b), 1);
-    for (int r = 0; r < 3; ++r) ptx::mbar_init(region_bar(r), 128);
+    for (int r = 0; r < 3; ++r) ptx::mbar_init(region_bar(r), kEpiThreads);
     ptx::mbar_init(drain_bar, 1);
     ptx::fence_mbar_init();
     *s_abort = 0;
@@ -214,7 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc += mt * n_tiles;
       s_prefix[e + 1] = acc;
     }
-    if (bad) raise_device_error(MOE_DEVERR_LAYOUT);
+    if (bad) {
+      // Tiles would straddle groups (and the output buffers): do no work.
+      raise_device_error(MOE_DEVERR_LAYOUT);
+      for (int e = 0; e < p.E; ++e) s_prefix[e + 1] = 0;
+    }
   }
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
@@ -301,14 +513,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++j) {
         TileInfo ti;
         decode_tile<MODE>(p, s_prefix, t, e_hint, ti);
-        const int other = (j & 1) ? 2 : 0;
+        const int own = (j & 1) ? 2 : 0;
         // Wait until both regions of this tile were drained by the epilogue.
         if (!gemm::wait_bar(region_bar(1), (uses[1] & 1u) ^ 1u, s_abort)) break;
-        if (!gemm::wait_bar(region_bar(other), (uses[other] & 1u) ^ 1u, s_abort)) break;
+        if (!gemm::wait_bar(region_bar(own), (uses[own] & 1u) ^ 1u, s_abort)) break;
         uses[1]++;
-        uses[other]++;
+        uses[own]++;
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + ((j & 1) ? 128u : 0u);
+        const uint32_t d_tmem = tmem_base + ((j & 1) ? (uint32_t)kAcc1Col : 0u);
         for (int kb = 0; kb < ti.k_iters; ++kb) {
           if (!gemm::wait_bar(full_bar(stage), phase, s_abort)) {
             ok = false;
@@ -352,8 +564,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
-    const int r = q * 32 + lane;
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;   // chunk parity (fused: two warps per quarter)
+    constexpr int NSH = L::kEpiWarps == 8 ? 1 : 2;  // shared chunks drained per warp
+    float* xs = reinterpret_cast<float*>(smem + L::kXposeOffset) + (warp - 2) * kXposeWords;
+    uint8_t* gu_stage = smem + L::kGuOffset + (warp - 2) * 32 * kGuRowBytes;
+    const uint32_t tl_lanes = tmem_base + ((uint32_t)(q * 32) << 16);
     int e_hint = 0;
     int j = 0;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++j) {
@@ -362,176 +578,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!gemm::wait_bar(tfull_bar(j & 1), (uint32_t)((j >> 1) & 1), s_abort)) break;
       ptx::tc_fence_after();
       const bool odd = (j & 1) != 0;
-      const int other = odd ? 2 : 0;
-      const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
-      // Tile-local column ranges: the shared region [128,256) holds local cols
-      // [128,256) for even tiles and [0,128) for odd tiles.
-      const int shared_lo = odd ? 0 : 128;
-      const int other_lo = odd ? 128 : 0;
-      const bool has_acc = ti.k_iters > 0;
-      float sh[128];  // the shared region, drained first
-      if (has_acc) {
+      // Drain this warp's part of the shared region [192, 256) (TMEM columns
+      // 192 + 32h for the fused kernels, all 64 for the plain ones) and hand
+      // the region back to the MMA thread.
+      float sh[32 * NSH];
+      if (ti.k_iters > 0) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < NSH; ++c) {
           uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(tl + 128 + c * 32, v);
+          ptx::tmem_ld_32x32b_x32(tl_lanes + kAcc1Col + (NSH == 1 ? 32 * h : 32 * c), v);
           ptx::tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) sh[c * 32 + i] = __uint_as_float(v[i]);
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) sh[i] = 0.f;
+        for (int i = 0; i < 32 * NSH; ++i) sh[i] = 0.f;
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(region_bar(1));
-
-      const long long lrow = (long long)ti.mt * BM + r;
-      if (MODE == WGRAD) {
-        __nv_bfloat16* crow = p.C + (long long)ti.e * p.c_group_stride + lrow * p.ldc +
-                              (long long)ti.nt * BN;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) gemm::store32_bf16(crow + shared_lo + c * 32, sh + c * 32);
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float f[32];
-          if (has_acc) {
-            uint32_t v[32];
-            ptx::tmem_ld_32x32b_x32(tl + (odd ? 256 : 0) + c * 32, v);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) f[i] = 0.f;
-          }
-          gemm::store32_bf16(crow + other_lo + c * 32, f);
-        }
-      } else {
-        const bool row_ok = lrow < ti.rows;
-        const long long grow = ti.row0 + lrow;
-        if (EPI == EPI_STORE) {
-          __nv_bfloat16* crow = p.C + grow * p.ldc + (long long)ti.nt * BN;
-          const int ncol = p.N - ti.nt * BN;  // valid columns in this tile
-          if (row_ok) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              if (shared_lo + c * 32 < ncol) gemm::store32_bf16(crow + shared_lo + c * 32, sh + c * 32);
-          }
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            ptx::tmem_ld_32x32b_x32(tl + (odd ? 256 : 0) + c * 32, v);
-            ptx::tmem_ld_wait();
-            float f[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-            if (row_ok && other_lo + c * 32 < ncol) gemm::store32_bf16(crow + other_lo + c * 32, f);
-          }
-        } else if (EPI == EPI_SWIGLU_FWD) {
-          // Tile-local cols [0,128) are gate, [128,256) are up, for F-columns
-          // n0 .. n0+127. The shared region holds up (even) or gate (odd).
-          const float pr = row_ok ? p.p_rows[grow] : 0.f;
-          const long long n0 = (long long)ti.nt * (BN / 2);
-          const long long F = p.F;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            ptx::tmem_ld_32x32b_x32(tl + (odd ? 256 : 0) + c * 32, v);
-            ptx::tmem_ld_wait();
-            float g[32], u[32], h[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float o = __uint_as_float(v[i]);
-              g[i] = odd ? sh[c * 32 + i] : o;
-              u[i] = odd ? o : sh[c * 32 + i];
-              h[i] = g[i] * gemm::sigmoidf_fast(g[i]) * u[i] * pr;
-            }
-            const long long col = n0 + c * 32;
-            if (row_ok) {
-              gemm::store32_bf16(p.GU + grow * 2 * F + col, g);
-              gemm::store32_bf16(p.GU + grow * 2 * F + F + col, u);
-              quant_row32(h, p.q_row + grow * p.q_row_ld + col,
-                          p.s_row + mx_scale_offset(grow, col >> 5, p.q_row_ld));
-            }
-            // column-wise blocks: the warp's 32 rows of each column
-#pragma unroll 4
-            for (int i = 0; i < 32; ++i) {
-              uint32_t sb;
-              const uint32_t code = quant_col_lane(h[i], sb);
-              const long long f = col + i;
-              const long long rb = (ti.row0 + (long long)ti.mt * BM + q * 32);
-              p.q_col[f * p.q_col_ld + rb + lane] = (uint8_t)code;
-              if (lane == 0) p.s_col[mx_scale_offset(f, rb >> 5, p.q_col_ld)] = (uint8_t)sb;
-            }
-          }
-        } else {  // EPI_SWIGLU_BWD: accumulator = dH for F-columns [nt*256, +256)
-          const float pr = row_ok ? p.p_rows[grow] : 0.f;
-          const long long F = p.F;
-          const int ncol = p.N - ti.nt * BN;
-          float dp = 0.f;
-          const long long rb = ti.row0 + (long long)ti.mt * BM + q * 32;
-#pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            const int lo = half == 0 ? shared_lo : other_lo;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              float dh[32];
-              if (half == 0) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) dh[i] = sh[c * 32 + i];
-              } else {
-                uint32_t v[32];
-                ptx::tmem_ld_32x32b_x32(tl + (odd ? 256 : 0) + c * 32, v);
-                ptx::tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) dh[i] = __uint_as_float(v[i]);
-              }
-              if (lo + c * 32 >= ncol) continue;  // N tail (uniform across the warp)
-              const long long col = (long long)ti.nt * BN + lo + c * 32;
-              float g[32], u[32], dg[32], du[32];
-              if (row_ok) {
-                gemm::load32_bf16(p.GU + grow * 2 * F + col, g);
-                gemm::load32_bf16(p.GU + grow * 2 * F + F + col, u);
-              } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) g[i] = u[i] = 0.f;
-              }
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const float s = gemm::sigmoidf_fast(g[i]);
-                const float silu = g[i] * s;
-                dp = fmaf(dh[i], silu * u[i], dp);
-                const float da = dh[i] * pr;
-                dg[i] = da * u[i] * s * (1.f + g[i] * (1.f - s));
-                du[i] = da * silu;
-              }
-              if (row_ok) {
-                quant_row32(dg, p.q_row + grow * p.q_row_ld + col,
-                            p.s_row + mx_scale_offset(grow, col >> 5, p.q_row_ld));
-                quant_row32(du, p.q_row + grow * p.q_row_ld + F + col,
-                            p.s_row + mx_scale_offset(grow, (F + col) >> 5, p.q_row_ld));
-              }
-#pragma unroll 4
-              for (int i = 0; i < 32; ++i) {
-                uint32_t sb1, sb2;
-                const uint32_t c1 = quant_col_lane(dg[i], sb1);
-                const uint32_t c2 = quant_col_lane(du[i], sb2);
-                const long long f = col + i;
-                p.q_col[f * p.q_col_ld + rb + lane] = (uint8_t)c1;
-                p.q_col[(F + f) * p.q_col_ld + rb + lane] = (uint8_t)c2;
-                if (lane == 0) {
-                  p.s_col[mx_scale_offset(f, rb >> 5, p.q_col_ld)] = (uint8_t)sb1;
-                  p.s_col[mx_scale_offset(F + f, rb >> 5, p.q_col_ld)] = (uint8_t)sb2;
-                }
-              }
-            }
-          }
-          if (row_ok) p.dp_part[grow * p.n_part + ti.nt] = dp;
-        }
-      }
+      epilogue_tile<MODE, EPI>(p, ti, odd, h, sh, tl_lanes + (odd ? (uint32_t)kAcc1Col : 0u), q,
+                               lane, xs, gu_stage);
       ptx::tc_fence_before();
-      ptx::mbar_arrive(region_bar(other));
+      ptx::mbar_arrive(region_bar(odd ? 2 : 0));
     }
   }
   ptx::tc_fence_before();
@@ -545,17 +614,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int MODE, int EPI>
 static int launch(const CUtensorMap& ta, const CUtensorMap& tb, const MxParams& p,
                   long long tiles_bound, cudaStream_t st) {
+  using L = Cfg<EPI != EPI_STORE>;
   auto kern = grouped_gemm_mxf8_kernel<MODE, EPI>;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
     attr_set = true;
   }
   long long grid = tiles_bound < gemm::num_sms() ? tiles_bound : gemm::num_sms();
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, kThreads, kSmemAlloc, st>>>(ta, tb, p);
+  kern<<<(unsigned)grid, L::kThreads, L::kSmemAlloc, st>>>(ta, tb, p);
   return launch_status();
 }
 
@@ -698,7 +768,7 @@ extern "C" int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t
   p.s_col = sdy1_col;
   p.q_col_ld = rows;
   p.dp_part = dp_part;
-  p.n_part = (F + MX::BN - 1) / MX::BN;
+  p.n_part = 2 * ((F + MX::BN - 1) / MX::BN);  // two epilogue warps per row and tile
   CUtensorMap ta, tb;
   if (!MX::u8_map(&ta, dy2q, rows, H) || !MX::u8_map(&tb, w2q, (long long)E * F, H)) return MOE_ERR_CUDA;
   long long bound = (rows / MX::BM + E) * (long long)((F + MX::BN - 1) / MX::BN);

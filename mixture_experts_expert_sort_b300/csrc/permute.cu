@@ -132,8 +132,13 @@ __global__ void __launch_bounds__(kPlanWarps * 32)
   }
 }
 
-// xp[dest[t*k+j]] = x[t]; padding rows zero. One warp per token; the last
-// ceil(E / 8) blocks zero the padding rows, one warp per expert.
+// xp[dest[t*k+j]] = x[t]; padding rows zero. One warp per token, four
+// independent 16-byte loads in flight per lane before the k scattered
+// stores. The last blocks zero the padding rows: kPadWarps warps per expert,
+// each taking every kPadWarps-th padding row of its expert. With xp NULL
+// only the per-row routing weights p_rows are written.
+constexpr int kPadWarps = 32;
+
 __global__ void __launch_bounds__(256)
     permute_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ dest,
                    const int32_t* __restrict__ offsets, const int32_t* __restrict__ counts,
@@ -141,12 +146,14 @@ __global__ void __launch_bounds__(256)
                    float* __restrict__ p_rows, int tok_blocks) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if ((int)blockIdx.x >= tok_blocks) {
-    int e = (blockIdx.x - tok_blocks) * 8 + warp;
+    const int gw = (blockIdx.x - tok_blocks) * 8 + warp;
+    const int e = gw / kPadWarps, part = gw % kPadWarps;
     if (e >= E) return;
-    long long r0 = (long long)offsets[e] + counts[e], r1 = offsets[e + 1];
+    const long long r0 = (long long)offsets[e] + counts[e], r1 = offsets[e + 1];
     const uint4 z = make_uint4(0, 0, 0, 0);
-    for (long long r = r0; r < r1; ++r) {
-      for (int v = lane; v < HV; v += 32) xp[r * HV + v] = z;
+    for (long long r = r0 + part; r < r1; r += kPadWarps) {
+      if (xp)
+        for (int v = lane; v < HV; v += 32) xp[r * HV + v] = z;
       if (p_rows && lane == 0) p_rows[r] = 0.f;
     }
     return;
@@ -155,14 +162,27 @@ __global__ void __launch_bounds__(256)
     int d[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) d[j] = (j < k) ? dest[t * k + j] : -1;
+    if (p_rows && lane < k && d[lane] >= 0) p_rows[d[lane]] = w[t * k + lane];
+    if (!xp) continue;
     const uint4* xr = x + t * HV;
-    for (int v = lane; v < HV; v += 32) {
-      uint4 val = xr[v];
+    int v = lane;
+    for (; v + 96 < HV; v += 128) {
+      uint4 val[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) val[u] = __ldcs(xr + v + 32 * u);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (d[j] >= 0) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) xp[(long long)d[j] * HV + v + 32 * u] = val[u];
+        }
+    }
+    for (; v < HV; v += 32) {
+      const uint4 val = __ldcs(xr + v);
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         if (d[j] >= 0) xp[(long long)d[j] * HV + v] = val;
     }
-    if (p_rows && lane < k && d[lane] >= 0) p_rows[d[lane]] = w[t * k + lane];
   }
 }
 
@@ -177,6 +197,8 @@ __device__ __forceinline__ void acc_bf16x8(float* acc, const uint4& v, float s) 
 }
 
 // out[t] = sum_j w[t,j] * y[dest[t*k+j]], fp32 in slot order, one rounding.
+// One warp per token; each lane issues the k row loads of two 16-byte
+// vectors before it sums them.
 __global__ void __launch_bounds__(256)
     unpermute_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ dest,
                      const float* __restrict__ w, int T, int HV, int k, uint4* __restrict__ out) {
@@ -189,16 +211,28 @@ __global__ void __launch_bounds__(256)
       d[j] = (j < k) ? dest[t * k + j] : -1;
       s[j] = (j < k) ? (w ? w[t * k + j] : 1.f) : 0.f;
     }
-    for (int v = lane; v < HV; v += 32) {
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int v0 = lane; v0 < HV; v0 += 64) {
+      const bool two = v0 + 32 < HV;
+      uint4 in[2][8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (d[j] >= 0) acc_bf16x8(acc, y[(long long)d[j] * HV + v], s[j]);
-      uint4 o;
-      __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+      for (int j = 0; j < 8; ++j) {
+        const bool ok = d[j] >= 0;
+        in[0][j] = ok ? __ldcs(y + (long long)d[j] * HV + v0) : make_uint4(0, 0, 0, 0);
+        in[1][j] = (ok && two) ? __ldcs(y + (long long)d[j] * HV + v0 + 32) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) oh[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-      out[t * HV + v] = o;
+      for (int h = 0; h < 2; ++h) {
+        if (h == 1 && !two) break;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (d[j] >= 0) acc_bf16x8(acc, in[h][j], s[j]);
+        uint4 o;
+        __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) oh[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+        out[t * HV + v0 + 32 * h] = o;
+      }
     }
   }
 }
@@ -276,13 +310,14 @@ extern "C" int moe_permute(const void* x, const int32_t* dest, const int32_t* of
                            const int32_t* counts, const float* w, int T, int H, int E, int k,
                            void* xp, float* p_rows, moe_stream_t stream) {
   if (T < 0 || H < 8 || H % 8 || E < 1 || k < 1 || k > 8 || k > E) return MOE_ERR_ARG;
-  if (!offsets || !counts || !xp || (T > 0 && (!x || !dest))) return MOE_ERR_ARG;
+  if (!offsets || !counts || (T > 0 && !dest)) return MOE_ERR_ARG;
   if ((w == nullptr) != (p_rows == nullptr)) return MOE_ERR_ARG;
-  if ((x && !aligned16(x)) || !aligned16(xp)) return MOE_ERR_ARG;
+  if (!xp && !p_rows) return MOE_ERR_ARG;  // nothing to write
+  if (xp && ((T > 0 && !x) || (x && !aligned16(x)) || !aligned16(xp))) return MOE_ERR_ARG;
   int HV = H / 8;
   long long tb = ((long long)T + 7) / 8;
   if (tb > 148 * 16) tb = 148 * 16;
-  int pad_blocks = (E + 7) / 8;
+  int pad_blocks = (E * kPadWarps + 7) / 8;
   permute_kernel<<<(unsigned)(tb + pad_blocks), 256, 0, (cudaStream_t)stream>>>(
       static_cast<const uint4*>(x), dest, offsets, counts, w, T, HV, E, k,
       static_cast<uint4*>(xp), p_rows, (int)tb);
