@@ -42,7 +42,12 @@ enum Mode { FPROP = 0, WGRAD = 1 };
 enum Epi { EPI_STORE = 0, EPI_SWIGLU_FWD = 1, EPI_SWIGLU_BWD = 2 };
 
 constexpr int BM = 128;
-constexpr int BK = 64;  // BF16: 64 elements = 128 bytes = one swizzle row
+// BF16 K per stage: 64 elements = 128 bytes = one 128-byte swizzle row.
+// (32-element stages with 64-byte rows allow a deeper ring but double the
+// TMA row requests of K-major operands, which measured slower.)
+constexpr int BK = 64;
+constexpr int kKRowBytes = BK * 2;            // one K-major row of a stage
+constexpr int kKAtomBytes = 8 * kKRowBytes;   // 8-row swizzle atom (K-major)
 constexpr int kThreads = 192;
 constexpr int kMaxGroups = 256;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
@@ -77,6 +82,7 @@ struct Smem {
   static constexpr int kPrefixOffset = kMiscOffset + 16;
   static constexpr int kBytes = kPrefixOffset + (kMaxGroups + 1) * 4;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 B
+  static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
 struct TileInfo {
@@ -274,11 +280,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           armed_phase[stage] = phase;
           const int k0 = kb * BK;
           if (MODE == FPROP) {
-            // A: rows of the group, K-major, one box of 128 rows x 64 K.
+            // A: rows of the group, K-major, one box of 128 rows x BK.
             ptx::tma_load_2d(a_dst, &tmA, k0, (int)(ti.row0 + (long long)ti.mt * BM),
                              full_bar(stage));
             if (B_MN) {
-              // B_e stored [K, N]: BN/64 chunks of [64 K rows][64 N].
+              // B_e stored [K, N]: BN/64 chunks of [BK K rows][64 N].
 #pragma unroll
               for (int c = 0; c < BN / 64; ++c) {
                 const int h = c / (BN / 128), off = (c % (BN / 128)) * 64;
@@ -287,11 +293,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  full_bar(stage));
               }
             } else {
-              // B_e stored [N, K]: two boxes of BN/2 rows x 64 K.
+              // B_e stored [N, K]: two boxes of BN/2 rows x BK.
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
                 const int n = b_half_col<EPI, BN>(p, ti.nt, h);
-                ptx::tma_load_2d(b_dst + h * (BN / 2) * 128, &tmB, k0, ti.e * p.N + n,
+                ptx::tma_load_2d(b_dst + h * (BN / 2) * kKRowBytes, &tmB, k0, ti.e * p.N + n,
                                  full_bar(stage));
               }
             }
@@ -347,11 +353,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (MODE == WGRAD || A_MN)
               da = ptx::smem_desc(a_addr + kk * 2048, BK * 128, 1024, ptx::kSwizzle128B);
             else
-              da = ptx::smem_desc(a_addr + kk * 32, 16, 1024, ptx::kSwizzle128B);
+              da = ptx::smem_desc(a_addr + kk * 32, 16, kKAtomBytes, ptx::kSwizzle128B);
             if (B_MN)
               db = ptx::smem_desc(b_addr + kk * 2048, BK * 128, 1024, ptx::kSwizzle128B);
             else
-              db = ptx::smem_desc(b_addr + kk * 32, 16, 1024, ptx::kSwizzle128B);
+              db = ptx::smem_desc(b_addr + kk * 32, 16, kKAtomBytes, ptx::kSwizzle128B);
             ptx::mma_bf16(d_tmem, da, db, idesc, (kb | kk) ? 1u : 0u);
           }
           ptx::mma_commit(empty_bar(stage));
@@ -512,7 +518,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 2-D row-major tensor [rows, cols] of `elem_bytes` elements, box [box_rows, box_cols],
 // 128-byte swizzle (box_cols * elem_bytes must be <= 128).
 static bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes,
-                      long long rows, long long cols, long long ld, int box_rows, int box_cols) {
+                      long long rows, long long cols, long long ld, int box_rows, int box_cols,
+                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -520,10 +527,13 @@ static bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, 
   cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+// K-major BF16 operands: 128-byte rows, 128-byte swizzle (matches kSwizzle128B).
+constexpr CUtensorMapSwizzle kKSwz = CU_TENSOR_MAP_SWIZZLE_128B;
 
 static int num_sms() {
   static int n = 0;
@@ -589,11 +599,11 @@ extern "C" int moe_grouped_gemm_bf16(int mode, const void* A, const void* B, int
     p.ldc = N;
     p.b_kmajor = b_layout;
     const bool bn256 = (N % 256) == 0;
-    if (!make_tmap(&ta, A, kBF16, 2, rows, K, K, BM, BK)) return MOE_ERR_CUDA;
+    if (!make_tmap(&ta, A, kBF16, 2, rows, K, K, BM, BK, kKSwz)) return MOE_ERR_CUDA;
     if (b_layout == 0) {
       if (!make_tmap(&tb, B, kBF16, 2, (long long)E * K, N, N, BK, 64)) return MOE_ERR_CUDA;
     } else {
-      if (!make_tmap(&tb, B, kBF16, 2, (long long)E * N, K, K, bn256 ? 128 : 64, BK))
+      if (!make_tmap(&tb, B, kBF16, 2, (long long)E * N, K, K, bn256 ? 128 : 64, BK, kKSwz))
         return MOE_ERR_CUDA;
     }
     long long bound = (rows / BM + E) * (long long)(N / 128);
@@ -639,7 +649,7 @@ extern "C" int moe_fc1_swiglu_bf16(const void* xp, const void* w1, const int32_t
   p.GU = static_cast<__nv_bfloat16*>(gu);
   p.Hout = static_cast<__nv_bfloat16*>(h);
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, xp, kBF16, 2, rows, H, H, BM, BK)) return MOE_ERR_CUDA;
+  if (!make_tmap(&ta, xp, kBF16, 2, rows, H, H, BM, BK, kKSwz)) return MOE_ERR_CUDA;
   if (!make_tmap(&tb, w1, kBF16, 2, (long long)E * H, 2 * F, 2 * F, BK, 64)) return MOE_ERR_CUDA;
   long long bound_base = rows / BM + E;
   cudaStream_t st = (cudaStream_t)stream;
@@ -675,9 +685,9 @@ extern "C" int moe_fc2_dgrad_swiglu_bwd_bf16(const void* dy2, const void* w2,
   p.n_part = moe_swiglu_bwd_parts(F);
   const bool bn256 = (F % 256) == 0;
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, dy2, kBF16, 2, rows, H, H, BM, BK)) return MOE_ERR_CUDA;
+  if (!make_tmap(&ta, dy2, kBF16, 2, rows, H, H, BM, BK, kKSwz)) return MOE_ERR_CUDA;
   // dH = dY2 * W2_e^T: B_e = W2_e stored [F, H] = [N, K], K-major.
-  if (!make_tmap(&tb, w2, kBF16, 2, (long long)E * F, H, H, bn256 ? 128 : 64, BK))
+  if (!make_tmap(&tb, w2, kBF16, 2, (long long)E * F, H, H, bn256 ? 128 : 64, BK, kKSwz))
     return MOE_ERR_CUDA;
   long long bound = (rows / BM + E) * (long long)(F / 128);
   cudaStream_t st = (cudaStream_t)stream;

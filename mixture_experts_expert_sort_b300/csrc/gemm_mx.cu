@@ -72,8 +72,10 @@ struct Cfg {
   // of all stages follow in a region of their own.
   static constexpr int kSfOffset = kStages * kStageBytes;
   static constexpr int kXposeOffset = kSfOffset + kStages * kSfStageBytes;
-  // Per-warp staging of the saved gate/up values the backward epilogue reads
-  // (cp.async): 32 rows x (64 B gate + 64 B up), rows padded to 144 B.
+  // Per-warp staging of gate/up: the backward epilogue reads the saved values
+  // through it (cp.async; 32 rows x (64 B gate + 64 B up), rows padded to
+  // 144 B); the forward epilogue writes its gate and up boxes (2 x 2 KB)
+  // there for TMA stores. 128-byte aligned.
   static constexpr int kGuOffset = kXposeOffset + (FUSED ? kEpiWarps * kXposeWords * 4 : 0);
   static constexpr int kBarOffset = kGuOffset + (FUSED ? kEpiWarps * 32 * kGuRowBytes : 0);
   // full[S], empty[S], tfull[2], region_empty[3], drain
@@ -269,7 +271,8 @@ __device__ __forceinline__ void unpack_bf16x32(const uint4* s, float* v) {
 template <int MODE, int EPI>
 __device__ __forceinline__ void epilogue_tile(const MxParams& p, const TileInfo& ti, bool odd,
                                               int h, const float* sh, uint32_t tl_tile, int q,
-                                              int lane, float* xs, uint8_t* gu_stage) {
+                                              int lane, float* xs, uint8_t* gu_stage,
+                                              const CUtensorMap* tm_gu) {
   const long long lrow = (long long)ti.mt * BM + q * 32 + lane;
   const bool has_acc = ti.k_iters > 0;
   if (MODE == WGRAD) {
@@ -311,9 +314,19 @@ __device__ __forceinline__ void epilogue_tile(const MxParams& p, const TileInfo&
       acc_chunk<1>(c, odd, h, sh, tl_tile, g);
       acc_chunk<1>(c + 4, odd, h, sh, tl_tile, u);
       const long long col = (long long)ti.nt * (BN / 2) + c * 32;
-      if (row_ok) {
-        gemm::store32_bf16(p.GU + grow * 2 * F + col, g);
-        gemm::store32_bf16(p.GU + grow * 2 * F + F + col, u);
+      // [g | u] in bf16: the warp's 32 x 32 gate and up boxes are staged in
+      // shared memory (row `lane` = 64 bytes each) and written by TMA.
+      if (lane == 0) ptx::bulk_wait_read_all();  // previous boxes have been read
+      __syncwarp();
+      gemm::store32_bf16(reinterpret_cast<__nv_bfloat16*>(gu_stage + lane * 64), g);
+      gemm::store32_bf16(reinterpret_cast<__nv_bfloat16*>(gu_stage + 2048 + lane * 64), u);
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t sa = ptx::smem_u32(gu_stage);
+        ptx::tma_store_2d(tm_gu, (int)col, (int)rb, sa);
+        ptx::tma_store_2d(tm_gu, (int)(F + col), (int)rb, sa + 2048);
+        ptx::bulk_commit_group();
       }
 #pragma unroll
       for (int i = 0; i < 32; ++i) g[i] = g[i] * gemm::sigmoidf_fast(g[i]) * u[i] * pr;  // h
@@ -375,7 +388,8 @@ __device__ __forceinline__ void epilogue_tile(const MxParams& p, const TileInfo&
 template <int MODE, int EPI>
 __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
     grouped_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA,
-                             const __grid_constant__ CUtensorMap tmB, const MxParams p) {
+                             const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmC, const MxParams p) {
   using L = Cfg<EPI != EPI_STORE>;
   constexpr int kStages = L::kStages;
   constexpr int kSfOffset = L::kSfOffset;
@@ -598,10 +612,12 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(region_bar(1));
       epilogue_tile<MODE, EPI>(p, ti, odd, h, sh, tl_lanes + (odd ? (uint32_t)kAcc1Col : 0u), q,
-                               lane, xs, gu_stage);
+                               lane, xs, gu_stage, &tmC);
       ptx::tc_fence_before();
       ptx::mbar_arrive(region_bar(odd ? 2 : 0));
     }
+    // Bulk stores must be complete before this CTA's shared memory goes away.
+    if (EPI == EPI_SWIGLU_FWD && lane == 0) ptx::bulk_wait_all();
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -612,8 +628,8 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
 }
 
 template <int MODE, int EPI>
-static int launch(const CUtensorMap& ta, const CUtensorMap& tb, const MxParams& p,
-                  long long tiles_bound, cudaStream_t st) {
+static int launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                  const MxParams& p, long long tiles_bound, cudaStream_t st) {
   using L = Cfg<EPI != EPI_STORE>;
   auto kern = grouped_gemm_mxf8_kernel<MODE, EPI>;
   static bool attr_set = false;
@@ -625,7 +641,7 @@ static int launch(const CUtensorMap& ta, const CUtensorMap& tb, const MxParams& 
   }
   long long grid = tiles_bound < gemm::num_sms() ? tiles_bound : gemm::num_sms();
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, L::kThreads, L::kSmemAlloc, st>>>(ta, tb, p);
+  kern<<<(unsigned)grid, L::kThreads, L::kSmemAlloc, st>>>(ta, tb, tc, p);
   return launch_status();
 }
 
@@ -684,14 +700,14 @@ extern "C" int moe_grouped_gemm_mxfp8(int mode, const uint8_t* a, const uint8_t*
     p.b_row_stride = b_row_stride;
     p.b_k_stride = b_k_stride;
     long long bound = (a_rows / MX::BM + E) * (long long)((N + MX::BN - 1) / MX::BN);
-    return MX::launch<FPROP, EPI_STORE>(ta, tb, p, bound, st);
+    return MX::launch<FPROP, EPI_STORE>(ta, tb, tb, p, bound, st);
   }
   if (mode == MOE_GEMM_WGRAD) {
     if (M < MX::BM || M % MX::BM || N < MX::BN || N % MX::BN || M > a_rows || N > b_rows || a_cols != b_cols)
       return MOE_ERR_ARG;
     p.c_group_stride = (long long)M * N;
     long long bound = (long long)E * (M / MX::BM) * (N / MX::BN);
-    return MX::launch<WGRAD, EPI_STORE>(ta, tb, p, bound, st);
+    return MX::launch<WGRAD, EPI_STORE>(ta, tb, tb, p, bound, st);
   }
   return MOE_ERR_ARG;
 }
@@ -727,11 +743,15 @@ extern "C" int moe_fc1_swiglu_mxfp8(const uint8_t* xq, const uint8_t* sx, long l
   p.q_col = hq_col;
   p.s_col = sh_col;
   p.q_col_ld = rows;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   if (!MX::u8_map(&ta, xq, rows, H) || !MX::u8_map(&tb, w1t, 2LL * F, (long long)E * H))
     return MOE_ERR_CUDA;
+  // [g | u] output, written by TMA in 32 x 32 boxes
+  if (!gemm::make_tmap(&tc, gu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, 2LL * F, 2LL * F, 32,
+                       32, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return MOE_ERR_CUDA;
   long long bound = (rows / MX::BM + E) * (long long)(F / 128);
-  return MX::launch<FPROP, EPI_SWIGLU_FWD>(ta, tb, p, bound, (cudaStream_t)stream);
+  return MX::launch<FPROP, EPI_SWIGLU_FWD>(ta, tb, tc, p, bound, (cudaStream_t)stream);
 }
 
 extern "C" int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t* sdy2,
@@ -772,5 +792,5 @@ extern "C" int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t
   CUtensorMap ta, tb;
   if (!MX::u8_map(&ta, dy2q, rows, H) || !MX::u8_map(&tb, w2q, (long long)E * F, H)) return MOE_ERR_CUDA;
   long long bound = (rows / MX::BM + E) * (long long)((F + MX::BN - 1) / MX::BN);
-  return MX::launch<FPROP, EPI_SWIGLU_BWD>(ta, tb, p, bound, (cudaStream_t)stream);
+  return MX::launch<FPROP, EPI_SWIGLU_BWD>(ta, tb, tb, p, bound, (cudaStream_t)stream);
 }

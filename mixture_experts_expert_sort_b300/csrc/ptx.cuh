@@ -84,6 +84,37 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// 2-D tiled tensor copy shared -> global (bulk-group completion). The
+// source must have been written before a proxy fence (fence_proxy_async).
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t c0, int32_t c1, uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(c0), "r"(c1), "r"(src)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until the bulk stores committed by this thread have finished reading
+// shared memory (their source may then be overwritten).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until the bulk stores committed by this thread have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (TMA) before a bulk copy reads them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 16-byte asynchronous copy global -> shared (L2 only), and its group
 // bookkeeping: commit the copies issued so far, wait until all have landed.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
@@ -186,7 +217,7 @@ __device__ __forceinline__ void tmem_ld_wait() {
 // ------------------------------------------------------------ descriptors
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
 // stride byte offsets (all >> 4), descriptor version 1 at bits 46-47 and the
-// swizzle mode at bits 61-63 (2 = 128-byte swizzle, 0 = none).
+// swizzle mode at bits 61-63 (2 = 128-byte, 4 = 64-byte swizzle, 0 = none).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes,
                                               uint32_t sbo_bytes, uint32_t swizzle) {
   uint64_t d = 0;
@@ -199,6 +230,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes,
 }
 
 constexpr uint32_t kSwizzle128B = 2;
+constexpr uint32_t kSwizzle64B = 4;
 constexpr uint32_t kSwizzleNone = 0;
 
 // Instruction descriptor, kind::f16 with BF16 A/B and FP32 D.

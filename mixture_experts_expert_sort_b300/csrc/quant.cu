@@ -10,8 +10,9 @@
 // (r, b) loads its row's 32-value block straight from global memory (the
 // warp reads 8 rows x 256 contiguous bytes), quantises it row-wise in
 // registers and parks the values in shared memory; after one barrier thread c
-// walks column c down the 32 rows for the column-wise block. HBM-bound:
-// 2 bytes read and 1 + 1/32 bytes written per element and direction.
+// walks column c down the 32 rows for the column-wise block. The next tile's
+// loads are issued before the current tile is processed. HBM-bound: 2 bytes
+// read and 1 + 1/32 bytes written per element and direction.
 #include "common.cuh"
 
 namespace moe {
@@ -20,6 +21,7 @@ namespace {
 constexpr int kQRows = 32;
 constexpr int kQCols = 128;
 constexpr int kQThreads = 128;
+constexpr int kQBand = 32;  // row tiles per band of the tile order
 
 __device__ __forceinline__ void quant32(const float* v, uint32_t sbyte, uint4& lo, uint4& hi) {
   uint32_t wds[8];
@@ -51,71 +53,120 @@ __device__ __forceinline__ float block_amax(const float* v) {
   return finite ? m : __uint_as_float(0x7F800000u);
 }
 
+// Staging tile for the column-wise pass: 32 rows of 132 floats. The row
+// pass writes 16-byte vectors with the 32-column block b rotated by 8b words
+// (conflict-free for 8 lanes per phase); the column pass reads one column
+// per thread, 32 banks per warp.
+constexpr int kQStride = 132;
+
+__device__ __forceinline__ int qtile_col(int b, int j) { return 32 * b + ((j + 8 * b) & 31); }
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* v) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int z = 0; z < 4; ++z) {
+    float2 f = __bfloat1622float2(h[z]);
+    v[2 * z] = f.x;
+    v[2 * z + 1] = f.y;
+  }
+}
+
+// One CTA works through tiles of 32 rows x 128 columns (grid-stride). Each
+// thread loads the next tile's 64 bytes of its row while it quantises the
+// current one, and the gather index is fetched two tiles ahead, so loads
+// stay in flight across the whole loop.
 __global__ void __launch_bounds__(kQThreads)
     mxfp8_quant_kernel(const __nv_bfloat16* __restrict__ in, long long rows, int cols,
                        long long ld, const int32_t* __restrict__ src, int src_div, int dirs,
                        uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
                        uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col) {
-  __shared__ float tile[kQRows][kQCols + 1];
+  __shared__ __align__(16) float tile[kQRows * kQStride];
   const int tid = threadIdx.x;
+  const int rr = tid >> 2, b = tid & 3;  // row-pass role: row rr, 32-column block b
   const long long row_tiles = rows / kQRows;
   const int col_tiles = cols / kQCols;
   const long long n_tiles = row_tiles * col_tiles;
-  for (long long tt = blockIdx.x; tt < n_tiles; tt += gridDim.x) {
-    const long long r0 = (tt / col_tiles) * kQRows;
-    const int c0 = (int)(tt % col_tiles) * kQCols;
-    // ---- row-wise: thread -> (row rr, block b)
-    {
-      const int rr = tid >> 2, b = tid & 3;
-      const long long r = r0 + rr;
-      long long in_row = r;
-      bool zero = false;
-      if (src) {
-        int s = src[r];
-        zero = s < 0;
-        in_row = zero ? 0 : (long long)(s / src_div);
-      }
-      float v[32];
-      if (zero) {
+  const long long step = gridDim.x;
+
+  // Tile order: bands of kQBand row tiles (1024 rows); inside a band the
+  // tiles run down the rows first, then across the columns. The CTAs in
+  // flight then cover a few thousand columns of about a thousand rows, which
+  // keeps the row reads, the row-wise writes and the column-wise writes
+  // (rows of the transposed output) in long contiguous runs.
+  auto tile_r0 = [&](long long t) -> long long {
+    const long long band = t / (kQBand * (long long)col_tiles);
+    const long long local = t - band * kQBand * (long long)col_tiles;
+    const long long rows_in = min((long long)kQBand, row_tiles - band * kQBand);
+    return (band * kQBand + local % rows_in) * kQRows;
+  };
+  auto tile_c0 = [&](long long t) -> int {
+    const long long band = t / (kQBand * (long long)col_tiles);
+    const long long local = t - band * kQBand * (long long)col_tiles;
+    const long long rows_in = min((long long)kQBand, row_tiles - band * kQBand);
+    return (int)(local / rows_in) * kQCols;
+  };
+  // Input row of this thread for tile t (-1: a zero row).
+  auto src_row = [&](long long t) -> long long {
+    const long long r = tile_r0(t) + rr;
+    if (!src) return r;
+    const int sv = src[r];
+    return sv < 0 ? -1 : (long long)(sv / src_div);
+  };
+  auto load = [&](long long t, long long in_row, uint4* raw) {
+    const int c0 = tile_c0(t);
+    if (in_row < 0) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.f;
-      } else {
-        const uint4* p = reinterpret_cast<const uint4*>(in + in_row * ld + c0 + 32 * b);
+      for (int q = 0; q < 4; ++q) raw[q] = make_uint4(0, 0, 0, 0);
+    } else {
+      const uint4* p = reinterpret_cast<const uint4*>(in + in_row * ld + c0 + 32 * b);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 u = p[q];
-          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-          for (int z = 0; z < 4; ++z) {
-            float2 f = __bfloat1622float2(h[z]);
-            v[8 * q + 2 * z] = f.x;
-            v[8 * q + 2 * z + 1] = f.y;
-          }
-        }
-      }
-      if (dirs & MOE_QUANT_ROWWISE) {
-        uint32_t sb = mx_scale_byte(block_amax(v));
-        uint4 lo, hi;
-        quant32(v, sb, lo, hi);
-        uint4* o = reinterpret_cast<uint4*>(q_row + r * cols + c0 + 32 * b);
-        o[0] = lo;
-        o[1] = hi;
-        s_row[mx_scale_offset(r, (c0 >> 5) + b, cols)] = (uint8_t)sb;
-      }
-      if (dirs & MOE_QUANT_COLWISE) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) tile[rr][32 * b + i] = v[i];
-      }
+      for (int q = 0; q < 4; ++q) raw[q] = __ldcs(p + q);
     }
-    if (dirs & MOE_QUANT_COLWISE) {
-      __syncthreads();
-      const int c = tid;
-      float v[32];
+  };
+
+  long long t = blockIdx.x;
+  uint4 raw[4];
+  long long row_next2 = 0;
+  if (t < n_tiles) {
+    load(t, src_row(t), raw);
+    if (t + step < n_tiles) row_next2 = src_row(t + step);
+  }
+  for (; t < n_tiles; t += step) {
+    const long long r0 = tile_r0(t);
+    const int c0 = tile_c0(t);
+    float v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = tile[i][c];
+    for (int q = 0; q < 4; ++q) bf16x8_to_f32(raw[q], v + 8 * q);
+    // Next tile's data (row index fetched one iteration ago) and the row index
+    // of the tile after it.
+    if (t + step < n_tiles) {
+      const long long row_next = row_next2;
+      if (t + 2 * step < n_tiles) row_next2 = src_row(t + 2 * step);
+      load(t + step, row_next, raw);
+    }
+    const long long r = r0 + rr;
+    if (dirs & MOE_QUANT_ROWWISE) {
       uint32_t sb = mx_scale_byte(block_amax(v));
       uint4 lo, hi;
       quant32(v, sb, lo, hi);
+      uint4* o = reinterpret_cast<uint4*>(q_row + r * cols + c0 + 32 * b);
+      o[0] = lo;
+      o[1] = hi;
+      s_row[mx_scale_offset(r, (c0 >> 5) + b, cols)] = (uint8_t)sb;
+    }
+    if (dirs & MOE_QUANT_COLWISE) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<float4*>(&tile[rr * kQStride + qtile_col(b, 4 * k)]) =
+            make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      __syncthreads();
+      const int c = tid, cb = c >> 5, cj = c & 31;
+      float w[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) w[i] = tile[i * kQStride + qtile_col(cb, cj)];
+      uint32_t sb = mx_scale_byte(block_amax(w));
+      uint4 lo, hi;
+      quant32(w, sb, lo, hi);
       uint4* o = reinterpret_cast<uint4*>(q_col + (long long)(c0 + c) * rows + r0);
       o[0] = lo;
       o[1] = hi;
