@@ -197,25 +197,27 @@ __device__ __forceinline__ void acc_bf16x8(float* acc, const uint4& v, float s) 
 }
 
 // out[t] = sum_j w[t,j] * y[dest[t*k+j]], fp32 in slot order, one rounding.
-// One warp per token; each lane issues the k row loads of two 16-byte
-// vectors before it sums them.
+// One warp per token; each lane issues the K row loads of two 16-byte
+// vectors before it sums them. K is a template parameter so that the load
+// buffers hold exactly K rows (occupancy: 2K vectors of registers per lane).
+template <int K>
 __global__ void __launch_bounds__(256)
     unpermute_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ dest,
-                     const float* __restrict__ w, int T, int HV, int k, uint4* __restrict__ out) {
+                     const float* __restrict__ w, int T, int HV, uint4* __restrict__ out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (long long t = (long long)blockIdx.x * 8 + warp; t < T; t += (long long)gridDim.x * 8) {
-    int d[8];
-    float s[8];
+    int d[K];
+    float s[K];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      d[j] = (j < k) ? dest[t * k + j] : -1;
-      s[j] = (j < k) ? (w ? w[t * k + j] : 1.f) : 0.f;
+    for (int j = 0; j < K; ++j) {
+      d[j] = dest[t * K + j];
+      s[j] = w ? w[t * K + j] : 1.f;
     }
     for (int v0 = lane; v0 < HV; v0 += 64) {
       const bool two = v0 + 32 < HV;
-      uint4 in[2][8];
+      uint4 in[2][K];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < K; ++j) {
         const bool ok = d[j] >= 0;
         in[0][j] = ok ? __ldcs(y + (long long)d[j] * HV + v0) : make_uint4(0, 0, 0, 0);
         in[1][j] = (ok && two) ? __ldcs(y + (long long)d[j] * HV + v0 + 32) : make_uint4(0, 0, 0, 0);
@@ -225,16 +227,22 @@ __global__ void __launch_bounds__(256)
         if (h == 1 && !two) break;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int j = 0; j < K; ++j)
           if (d[j] >= 0) acc_bf16x8(acc, in[h][j], s[j]);
         uint4 o;
         __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
 #pragma unroll
         for (int q = 0; q < 4; ++q) oh[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-        out[t * HV + v0 + 32 * h] = o;
+        __stcs(out + t * HV + v0 + 32 * h, o);
       }
     }
   }
+}
+
+template <int K>
+void launch_unpermute(const uint4* y, const int32_t* dest, const float* w, int T, int HV,
+                      uint4* out, unsigned blocks, cudaStream_t st) {
+  unpermute_kernel<K><<<blocks, 256, 0, st>>>(y, dest, w, T, HV, out);
 }
 
 }  // namespace
@@ -331,7 +339,19 @@ extern "C" int moe_unpermute(const void* y, const int32_t* dest, const float* w,
   if (!y || !dest || !out || !aligned16(y) || !aligned16(out)) return MOE_ERR_ARG;
   long long blocks = ((long long)T + 7) / 8;
   if (blocks > 148 * 16) blocks = 148 * 16;
-  unpermute_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
-      static_cast<const uint4*>(y), dest, w, T, H / 8, k, static_cast<uint4*>(out));
+  const uint4* yv = static_cast<const uint4*>(y);
+  uint4* ov = static_cast<uint4*>(out);
+  const unsigned nb = (unsigned)blocks;
+  cudaStream_t st = (cudaStream_t)stream;
+  switch (k) {
+    case 1: launch_unpermute<1>(yv, dest, w, T, H / 8, ov, nb, st); break;
+    case 2: launch_unpermute<2>(yv, dest, w, T, H / 8, ov, nb, st); break;
+    case 3: launch_unpermute<3>(yv, dest, w, T, H / 8, ov, nb, st); break;
+    case 4: launch_unpermute<4>(yv, dest, w, T, H / 8, ov, nb, st); break;
+    case 5: launch_unpermute<5>(yv, dest, w, T, H / 8, ov, nb, st); break;
+    case 6: launch_unpermute<6>(yv, dest, w, T, H / 8, ov, nb, st); break;
+    case 7: launch_unpermute<7>(yv, dest, w, T, H / 8, ov, nb, st); break;
+    default: launch_unpermute<8>(yv, dest, w, T, H / 8, ov, nb, st); break;
+  }
   return launch_status();
 }
