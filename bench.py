@@ -104,11 +104,12 @@ class Step:
     moe_layer_backward make, over the same workspace, with optional CUDA events
     between calls for the per-kernel breakdown."""
 
-    def __init__(self, wl, dev):
+    def __init__(self, wl, dev, router=False):
         from mixture_experts_expert_sort_b300 import binding as B
         from mixture_experts_expert_sort_b300.layer import MoELayer
         self.B = B
         self.wl = wl
+        self.router = router
         self.mx = wl.precision == "mxfp8"
         self.layer = MoELayer(wl.T, wl.H, wl.F, wl.E, wl.k, precision=wl.precision,
                               align=wl.align, device=dev)
@@ -118,9 +119,19 @@ class Step:
         self.nparts = self.P["dp"].numel() // self.rmax
         self.plan_ws = torch.empty(B.moe_permute_plan_workspace_size(wl.T, wl.E, wl.k),
                                    dtype=torch.uint8, device=dev)
+        if router:
+            # Router projection W_r [H, E], its gradient, the logits it produces,
+            # the aux statistics and the router workspace.
+            self.w_r = I.make_router_weights(wl, device=dev)
+            self.dw_r = torch.empty_like(self.w_r)
+            self.logits_r = torch.empty((wl.T, wl.E), dtype=torch.float32, device=dev)
+            self.aux = torch.empty(1 + 2 * wl.E, dtype=torch.float32, device=dev)
+            self.router_ws = torch.empty(B.moe_router_workspace_size(wl.T, wl.H, wl.E),
+                                         dtype=torch.uint8, device=dev)
         self.NAMES = [n for n, _ in self._ops(*([None] * 10))]
-        # kernels per step: the plan is three launches, every other call one
-        self.launches_per_step = len(self.NAMES) + 2
+        # kernels per step: the plan is three launches, the router forward five
+        # and its backward four, every other call one
+        self.launches_per_step = len(self.NAMES) + 2 + (7 if router else 0)
 
     def _ops(self, logits, x, w1, w2, dout, out, dx, dw1, dw2, dlogits):
         B, wl, P = self.B, self.wl, self.P
@@ -130,8 +141,14 @@ class Step:
         p = B.ptr
         RC = B.QUANT_ROWWISE | B.QUANT_COLWISE
         npart = self.nparts
+        if self.router:
+            first = ("router_fwd", lambda: L.moe_router_forward(
+                p(x), p(self.w_r), T, H, E, k, p(self.logits_r), p(P["idx"]), p(P["w"]),
+                p(self.aux), p(self.router_ws), self.router_ws.numel(), s))
+        else:
+            first = ("route", lambda: L.moe_route(p(logits), T, E, k, p(P["idx"]), p(P["w"]), s))
         ops = [
-            ("route", lambda: L.moe_route(p(logits), T, E, k, p(P["idx"]), p(P["w"]), s)),
+            first,
             ("plan", lambda: L.moe_permute_plan(
                 p(P["idx"]), T, E, k, wl.align, p(P["counts"]), p(P["offsets"]), p(P["dest"]),
                 p(P["src"]), R, p(self.plan_ws), self.plan_ws.numel(), s)),
@@ -210,6 +227,12 @@ class Step:
                 p(P["dp"]), npart, npart, p(P["dest"]), p(P["w"]), p(P["idx"]), T, E, k,
                 p(dlogits), s)),
         ]
+        if self.router:
+            # aux-loss gradient (coefficient 0.01), dX += dlogits W_r^T, dW_r
+            ops.append(("router_bwd", lambda: L.moe_router_backward(
+                p(x), p(self.w_r), p(self.logits_r), p(self.aux), p(dlogits), 0.01, T, H, E,
+                p(dlogits), p(dx), p(dx), p(self.dw_r), p(self.router_ws),
+                self.router_ws.numel(), s)))
         return ops
 
     def bind(self, *tensors):
@@ -249,6 +272,10 @@ def kernel_work(wl):
         "permute_dout": ("bytes", T * H * 2.0 + R * H * 2.0),
         "unpermute_dx": ("bytes", R * H * 2.0 + T * H * 2.0),
         "route_bwd": ("bytes", R * 4.0 * 2 + T * E * 4.0),
+        # router projection: read x and W_r, write logits (then route + aux read them)
+        "router_fwd": ("bytes", T * H * 2.0 + H * E * 2.0 + T * E * 4.0 * 3 + R * 8.0),
+        # aux gradient (logits, dlogits), dX read + write, x for dW_r, dW_r
+        "router_bwd": ("bytes", T * E * 4.0 * 3 + T * H * 2.0 * 3 + H * E * 2.0 * 2),
     }
 
 
@@ -407,7 +434,7 @@ def run_ours(args, wl, world, rank, local):
     dw1 = torch.empty((E, H, 2 * F), dtype=bf, device=dev)
     dw2 = torch.empty((E, F, H), dtype=bf, device=dev)
     dlogits = torch.empty((T, E), dtype=torch.float32, device=dev)
-    step = Step(wl, dev)
+    step = Step(wl, dev, router=args.router)
     step.bind(logits, x, w1, w2, dout, out, dx, dw1, dw2, dlogits)
 
     for _ in range(args.warmup):
@@ -520,7 +547,9 @@ def run_ours(args, wl, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 (mxfp8)" if mx else "bf16",
         "data": "synthetic (seeded, generated on the device)",
-        "config": config_of(wl),
+        "config": dict(config_of(wl), router=("router projection x W_r, top-k, aux "
+                                              "load-balancing loss and their backward included"
+                                              if args.router else "logits given (no router)")),
         "gemm_tflops": gemm_tflops,
         "gemm_frac_of_measured_peak": gemm_tflops / tensor_peak,
         "gemm_frac_of_spec": gemm_tflops / (4500.0 if mx else 2250.0),
@@ -553,6 +582,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling cases)")
     ap.add_argument("--experts", type=int, default=0, help="override E (profiling cases)")
+    ap.add_argument("--router", action="store_true",
+                    help="compute the logits with the router projection (x W_r) and add the "
+                         "aux load-balancing loss and the router backward to the step")
     args = ap.parse_args()
     wl = I.WORKLOADS[args.workload]
     if args.tokens or args.experts:

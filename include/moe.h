@@ -96,6 +96,50 @@ MOE_API int moe_route_backward(const float* dp, long long ld_dp, int n_part, con
                        float* dlogits, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Router projection and auxiliary load-balancing loss. "How MoE Architecture
+ * Cuts Costs and Boosts Efficiency: ...", the Router paragraph (a score for
+ * every expert per token; the top K are kept) and "Engineering Challenges of
+ * Efficient Training" (an auxiliary load-balancing loss added to the
+ * training objective penalises uneven expert load).
+ *
+ * moe_router_forward:
+ *   logits[t, e] = sum_h x[t, h] * w_r[h, e]   (fp32; H is summed in fixed slices
+ *                  that are added in order, so the result is deterministic)
+ *   idx, w       = moe_route(logits, k)
+ *   aux          = [L_aux, f_0..f_{E-1}, P_0..P_{E-1}] (fp32, 1 + 2E values) with
+ *                  f_e = #{(t, j): idx[t, j] = e} / (T*k), P_e = mean over t of
+ *                  softmax_e(logits[t, :]) over all E, L_aux = E * sum_e f_e * P_e
+ *                  (1 for perfectly balanced routing).
+ *   x [T, H] bf16 (16-byte aligned), w_r [H, E] bf16, logits [T, E] fp32 (out),
+ *   idx [T, k] int32 and w [T, k] fp32 (out), aux (out).
+ *   workspace: at least moe_router_workspace_size(T, H, E) bytes, 256-aligned.
+ *   Requires H % 64 == 0, 1 <= k <= min(E, 8), E <= 256.
+ *   Every sum over tokens is taken in a fixed order: results are
+ *   deterministic.
+ * moe_router_backward: given dlogits_route = dL/dlogits from the experts'
+ * path (moe_route_backward; may be NULL) and the weight aux_coeff of L_aux in
+ * the training loss,
+ *   dlogits[t, e] = dlogits_route[t, e]
+ *                   + aux_coeff * (E/T) * s[t, e] * (f_e - sum_i f_i * s[t, i])
+ *   (s = softmax(logits[t, :]); the top-k selection has no gradient),
+ *   dx_out[t, h]  = dx_in[t, h] + sum_e dlogits[t, e] * w_r[h, e]  (bf16;
+ *                   dx_in may be NULL or equal dx_out, e.g. the experts' dX),
+ *   dw_r[h, e]    = sum_t x[t, h] * dlogits[t, e]  (bf16).
+ *   logits and aux as written by moe_router_forward; dlogits [T, E] fp32 (out;
+ *   may be the same buffer as dlogits_route). w_r, dx_in and dx_out 16-byte
+ *   aligned.
+ */
+MOE_API size_t moe_router_workspace_size(int T, int H, int E);
+MOE_API int moe_router_forward(const void* x, const void* w_r, int T, int H, int E, int k,
+                               float* logits, int32_t* idx, float* w, float* aux,
+                               void* workspace, size_t workspace_bytes, moe_stream_t stream);
+MOE_API int moe_router_backward(const void* x, const void* w_r, const float* logits,
+                                const float* aux, const float* dlogits_route, float aux_coeff,
+                                int T, int H, int E, float* dlogits, const void* dx_in,
+                                void* dx_out, void* dw_r, void* workspace,
+                                size_t workspace_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Expert sort: the per-expert token lists and split sizes of
  * "Efficient MoE Training ...", §Challenge 1, built as a stable counting
  * sort of the T*k routed rows by expert.

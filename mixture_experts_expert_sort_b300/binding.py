@@ -47,6 +47,10 @@ SIGNATURES = {
                                   _p]),
     "moe_fc2_dgrad_swiglu_bwd_mxfp8": (_i, [_p, _p, _ll, _i, _p, _p, _p, _p, _p, _i, _i, _p, _p,
                                             _p, _p, _p, _p]),
+    "moe_router_workspace_size": (_sz, [_i, _i, _i]),
+    "moe_router_forward": (_i, [_p, _p, _i, _i, _i, _i, _p, _p, _p, _p, _p, _sz, _p]),
+    "moe_router_backward": (_i, [_p, _p, _p, _p, _p, C.c_float, _i, _i, _i, _p, _p, _p, _p, _p,
+                                 _sz, _p]),
     "moe_layer_workspace_size": (_sz, [_p]),
     "moe_layer_workspace_part": (_i, [_p, _i, C.POINTER(_sz), C.POINTER(_sz)]),
     "moe_layer_forward": (_i, [_p, _p, _p, _p, _p, _p, _p, _sz, _p]),
@@ -119,6 +123,51 @@ def moe_route_backward(dp, w, idx, E, dest=None, dlogits=None, stream=None):
                                     ptr(idx), T, E, k, ptr(dlogits), stream_handle(stream)),
            "moe_route_backward")
     return dlogits
+
+
+# ----------------------------------------------------------------- router
+
+def moe_router_workspace_size(T, H, E):
+    return int(lib().moe_router_workspace_size(T, H, E))
+
+
+def moe_router_forward(x, w_r, k, workspace=None, stream=None, out=None):
+    """logits = x @ w_r, top-k routing, aux load-balancing statistics.
+    Returns dict with logits [T,E], idx [T,k], w [T,k], aux [1+2E] (loss, f, P)."""
+    T, H = x.shape
+    E = w_r.shape[1]
+    dev = x.device
+    if out is None:
+        out = {"logits": torch.empty((T, E), dtype=torch.float32, device=dev),
+               "idx": torch.empty((T, k), dtype=torch.int32, device=dev),
+               "w": torch.empty((T, k), dtype=torch.float32, device=dev),
+               "aux": torch.empty(1 + 2 * E, dtype=torch.float32, device=dev)}
+    if workspace is None:
+        workspace = torch.empty(moe_router_workspace_size(T, H, E), dtype=torch.uint8, device=dev)
+    _check(lib().moe_router_forward(ptr(x), ptr(w_r), T, H, E, k, ptr(out["logits"]),
+                                    ptr(out["idx"]), ptr(out["w"]), ptr(out["aux"]),
+                                    ptr(workspace), workspace.numel(), stream_handle(stream)),
+           "moe_router_forward")
+    return out
+
+
+def moe_router_backward(x, w_r, logits, aux, dlogits_route, aux_coeff, dx_in=None, dx_out=None,
+                        dlogits=None, dw_r=None, workspace=None, stream=None):
+    T, H = x.shape
+    E = w_r.shape[1]
+    dev = x.device
+    dlogits = dlogits if dlogits is not None else torch.empty((T, E), dtype=torch.float32,
+                                                              device=dev)
+    dx_out = dx_out if dx_out is not None else torch.empty((T, H), dtype=torch.bfloat16,
+                                                           device=dev)
+    dw_r = dw_r if dw_r is not None else torch.empty((H, E), dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = torch.empty(moe_router_workspace_size(T, H, E), dtype=torch.uint8, device=dev)
+    _check(lib().moe_router_backward(ptr(x), ptr(w_r), ptr(logits), ptr(aux), ptr(dlogits_route),
+                                     float(aux_coeff), T, H, E, ptr(dlogits), ptr(dx_in),
+                                     ptr(dx_out), ptr(dw_r), ptr(workspace), workspace.numel(),
+                                     stream_handle(stream)), "moe_router_backward")
+    return dlogits, dx_out, dw_r
 
 
 # ------------------------------------------------------------ expert sort

@@ -2,6 +2,7 @@
 // that the device error word and other file-scope device symbols need no
 // relocatable device code.
 #include "route.cu"
+#include "router.cu"
 #include "permute.cu"
 #include "plan_static.cu"
 #include "quant.cu"

@@ -19,7 +19,8 @@ router logits fp32 N(0,1) [T,E]; upstream gradient dOut ~ N(0,1) bf16.
 ``finegrained`` adds a per-expert bias b_e = -1.2*ln(r_e) to the logits, with
 r a seeded permutation of 1..E (Zipf(s=1.2) log-popularity); the four experts
 with the largest r get b_e = -1e4 so that they receive no token at all.
-``long`` scales round(0.01*T) seeded rows of x by 100.
+``long`` scales round(0.01*T) seeded rows of x by 100. The optional router
+projection W_r [H, E] is N(0, 1/H) in bf16.
 
 Every tensor has its own seed (workload seed * 16 + tensor id), so a tensor's
 values do not depend on which other tensors were drawn.
@@ -68,7 +69,7 @@ WORKLOADS = {
     "long": Workload("long", 65536, 4096, 14336, 8, 2, "mxfp8", 1005, outlier_frac=0.01),
 }
 
-_X, _W1, _W2, _LOGITS, _DOUT, _BIAS_PERM, _OUTLIER_ROWS = range(7)
+_X, _W1, _W2, _LOGITS, _DOUT, _BIAS_PERM, _OUTLIER_ROWS, _WROUTER, _DLOGITS = range(9)
 
 
 def _gen(wl: Workload, tensor_id: int, device) -> torch.Generator:
@@ -128,6 +129,16 @@ def make_logits(wl: Workload, device="cpu") -> torch.Tensor:
 
 def make_dout(wl: Workload, device="cpu") -> torch.Tensor:
     return _normal((wl.T, wl.H), 1.0, wl, _DOUT, device, torch.bfloat16)
+
+
+def make_router_weights(wl: Workload, device="cpu") -> torch.Tensor:
+    """Router projection W_r [H, E] ~ N(0, 1/H) in bf16 (logits of order 1)."""
+    return _normal((wl.H, wl.E), wl.H ** -0.5, wl, _WROUTER, device, torch.bfloat16)
+
+
+def make_dlogits(wl: Workload, device="cpu") -> torch.Tensor:
+    """An upstream gradient for the router logits, fp32 N(0,1) [T, E]."""
+    return _normal((wl.T, wl.E), 1.0, wl, _DLOGITS, device, torch.float32)
 
 
 def make_all(wl: Workload, device="cpu") -> dict:

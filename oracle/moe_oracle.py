@@ -101,6 +101,55 @@ def route_backward(dp, w, idx, E):
 
 
 # ---------------------------------------------------------------------------
+# Router projection and auxiliary load-balancing loss
+# [MOEBIO Router paragraph: a score for every expert per token; MOEBIO
+#  "Engineering Challenges of Efficient Training": an auxiliary loss that
+#  penalises uneven expert load]
+# ---------------------------------------------------------------------------
+
+def router_logits(x, Wr):
+    """logits[t, e] = sum_h x[t, h] * Wr[h, e] (x [T, H], Wr [H, E])."""
+    return np.asarray(x, dtype=f64) @ np.asarray(Wr, dtype=f64)
+
+
+def softmax_all(logits):
+    """Softmax of every token's logits over all E experts."""
+    lg = np.asarray(logits, dtype=f64)
+    z = np.exp(lg - lg.max(axis=1, keepdims=True))
+    return z / z.sum(axis=1, keepdims=True)
+
+
+def aux_load_balance(logits, idx, E):
+    """Load-balancing loss L = E * sum_e f_e * P_e.
+
+    f_e = fraction of the routed (token, slot) pairs that go to expert e;
+    P_e = mean over tokens of the softmax probability of expert e. The loss is
+    1 for perfectly balanced routing and grows as load concentrates.
+    Returns (L, f [E], P [E]).
+    """
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    f = np.bincount(idx.reshape(-1), minlength=E).astype(f64) / (T * k)
+    P = softmax_all(logits).mean(axis=0)
+    return float(E * np.sum(f * P)), f, P
+
+
+def aux_load_balance_grad(logits, f):
+    """dL/dlogits with f held fixed (the selection has no gradient):
+    dL/dl[t, e] = (E / T) * s[t, e] * (f_e - sum_i f_i * s[t, i])."""
+    s = softmax_all(logits)
+    T, E = s.shape
+    c = (s * np.asarray(f, dtype=f64)[None, :]).sum(axis=1, keepdims=True)
+    return (E / T) * s * (np.asarray(f, dtype=f64)[None, :] - c)
+
+
+def router_backward(x, Wr, dlogits):
+    """Gradients of the projection: dx = dlogits @ Wr^T, dWr = x^T @ dlogits."""
+    dl = np.asarray(dlogits, dtype=f64)
+    return dl @ np.asarray(Wr, dtype=f64).T, np.asarray(x, dtype=f64).T @ dl
+
+
+# ---------------------------------------------------------------------------
 # Permutation into contiguous per-expert groups
 # [EMT §Challenge 1: per-expert token lists and ``split_sizes``]
 # ---------------------------------------------------------------------------

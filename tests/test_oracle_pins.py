@@ -434,3 +434,88 @@ def test_grouped_gemm_brute_force():
             for n in range(6):
                 want = sum(A[r, m] * Y[r, n] for r in range(r0, r1))
                 assert abs(W[e, m, n] - want) < 1e-12
+
+
+# ------------------------------------------------------- router and aux loss
+
+def test_router_logits_brute_force():
+    rng = np.random.default_rng(31)
+    x, Wr = rng.standard_normal((5, 7)), rng.standard_normal((7, 3))
+    ref = np.zeros((5, 3))
+    for t in range(5):
+        for e in range(3):
+            for h in range(7):
+                ref[t, e] += x[t, h] * Wr[h, e]
+    np.testing.assert_allclose(O.router_logits(x, Wr), ref, rtol=1e-13)
+
+
+def test_aux_loss_is_one_when_balanced():
+    # uniform probabilities (equal logits) and round-robin routing: f = P = 1/E
+    E, k, T = 8, 2, 64
+    idx = np.array([[(2 * t) % E, (2 * t + 1) % E] for t in range(T)])
+    L, f, P = O.aux_load_balance(np.zeros((T, E)), idx, E)
+    assert L == 1.0
+    np.testing.assert_array_equal(f, np.full(E, 1 / E))
+
+
+def test_aux_loss_all_on_one_expert_closed_form():
+    # every token picks expert 0 (k=1) with logit a against 0: L = E * P_0
+    E, T, a = 5, 10, 2.0
+    lg = np.zeros((T, E))
+    lg[:, 0] = a
+    L, f, P = O.aux_load_balance(lg, np.zeros((T, 1), dtype=int), E)
+    assert abs(L - E * np.exp(a) / (np.exp(a) + E - 1)) < 1e-14
+
+
+def test_aux_grad_finite_differences_and_row_sums():
+    rng = np.random.default_rng(32)
+    T, E, k = 6, 5, 2
+    lg = rng.standard_normal((T, E))
+    idx, _ = O.route(lg, k)
+    _, f, _ = O.aux_load_balance(lg, idx, E)
+    g = O.aux_load_balance_grad(lg, f)
+
+    def loss(l):  # f held fixed: the routing decision carries no gradient
+        return E * np.sum(f * O.softmax_all(l).mean(axis=0))
+    num = np.zeros_like(lg)
+    eps = 1e-6
+    for t in range(T):
+        for e in range(E):
+            lp, lm = lg.copy(), lg.copy()
+            lp[t, e] += eps
+            lm[t, e] -= eps
+            num[t, e] = (loss(lp) - loss(lm)) / (2 * eps)
+    np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-10)
+    np.testing.assert_allclose(g.sum(axis=1), 0.0, atol=1e-15)
+
+
+def test_router_backward_brute_force():
+    rng = np.random.default_rng(33)
+    T, H, E = 4, 6, 3
+    x, Wr, dl = rng.standard_normal((T, H)), rng.standard_normal((H, E)), rng.standard_normal((T, E))
+    dx, dW = O.router_backward(x, Wr, dl)
+    for t in range(T):
+        for h in range(H):
+            assert abs(dx[t, h] - sum(dl[t, e] * Wr[h, e] for e in range(E))) < 1e-12
+    for h in range(H):
+        for e in range(E):
+            assert abs(dW[h, e] - sum(x[t, h] * dl[t, e] for t in range(T))) < 1e-12
+
+
+def test_planted_aux_mistakes_are_caught(monkeypatch):
+    """An unnormalised softmax or a flipped sign in the aux gradient trips the
+    pins above (the balanced-loss value and the finite differences)."""
+    E, k, T = 4, 2, 8
+    idx = np.array([[(2 * t) % E, (2 * t + 1) % E] for t in range(T)])
+    real_softmax = O.softmax_all
+    with monkeypatch.context() as m:
+        m.setattr(O, "softmax_all", lambda l: np.exp(np.asarray(l, dtype=float)))
+        L, _, _ = O.aux_load_balance(np.zeros((T, E)), idx, E)
+    assert L != 1.0
+    rng = np.random.default_rng(35)
+    lg = rng.standard_normal((T, E))
+    f = np.full(E, 1.0 / E) + np.linspace(-0.1, 0.1, E)
+    good = O.aux_load_balance_grad(lg, f)
+    s = real_softmax(lg)
+    flipped = (E / T) * s * ((s * f).sum(axis=1, keepdims=True) - f)
+    assert np.linalg.norm(flipped - good) > 0.5 * np.linalg.norm(good)
