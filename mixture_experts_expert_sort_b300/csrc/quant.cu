@@ -6,174 +6,236 @@
 // master values quantised before each low-precision GEMM); the rule is the
 // OCP Microscaling (MX) v1.0 one for E4M3 elements and E8M0 scales.
 //
-// A CTA of 128 threads works on tiles of 32 rows x 128 columns. Thread
-// (r, b) loads its row's 32-value block straight from global memory (the
-// warp reads 8 rows x 256 contiguous bytes), quantises it row-wise in
-// registers and parks the values in shared memory; after one barrier thread c
-// walks column c down the 32 rows for the column-wise block. The next tile's
-// loads are issued before the current tile is processed. HBM-bound: 2 bytes
-// read and 1 + 1/32 bytes written per element and direction.
+// A CTA of 256 threads works on tiles of 32 rows x 256 columns held in a
+// ring of shared-memory tiles filled by cp.async: a row pass (one 32-value
+// block per thread) and a column pass (one word column = two columns per
+// thread). HBM-bound: 2 bytes read and 1 + 1/32 bytes written per element
+// and direction.
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kQRows = 32;
-constexpr int kQCols = 128;
-constexpr int kQThreads = 128;
-constexpr int kQBand = 32;  // row tiles per band of the tile order
+constexpr int kQCols = 256;      // tile width; a last tile of 128 columns is allowed
+constexpr int kQThreads = 256;
+constexpr int kQBand = 32;       // row tiles per band of the tile order
 
-__device__ __forceinline__ void quant32(const float* v, uint32_t sbyte, uint4& lo, uint4& hi) {
-  uint32_t wds[8];
-  if (sbyte == 0xFFu) {
+// Largest |value| of 32 bf16 (16 packed words) as bf16 bits; non-negative bf16
+// order like their bit patterns and Inf/NaN are the largest.
+__device__ __forceinline__ uint32_t amax_bf16x32(const uint32_t* w) {
+  uint32_t m = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) wds[i] = 0x7F7F7F7Fu;
-  } else {
-    float inv = mx_inv_scale(sbyte);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint32_t a = cvt_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv);
-      uint32_t b = cvt_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv);
-      wds[i] = a | (b << 16);
-    }
-  }
-  lo = make_uint4(wds[0], wds[1], wds[2], wds[3]);
-  hi = make_uint4(wds[4], wds[5], wds[6], wds[7]);
+  for (int i = 0; i < 16; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+  return max(m >> 16, m & 0xFFFFu);
 }
 
-__device__ __forceinline__ float block_amax(const float* v) {
-  float m = 0.f;
-  bool finite = true;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    float a = fabsf(v[i]);
-    finite = finite && (a <= 3.402823466e38f);  // false for Inf and NaN
-    m = fmaxf(m, a);
-  }
-  return finite ? m : __uint_as_float(0x7F800000u);
+__device__ __forceinline__ uint32_t scale_of_bf16_amax(uint32_t abits) {
+  return abits >= 0x7F80u ? 0xFFu : mx_scale_byte(__uint_as_float(abits << 16));
 }
 
-// Staging tile for the column-wise pass: 32 rows of 132 floats. The row
-// pass writes 16-byte vectors with the 32-column block b rotated by 8b words
-// (conflict-free for 8 lanes per phase); the column pass reads one column
-// per thread, 32 banks per warp.
-constexpr int kQStride = 132;
-
-__device__ __forceinline__ int qtile_col(int b, int j) { return 32 * b + ((j + 8 * b) & 31); }
-
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* v) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+// E4M3 codes of 32 bf16 values (packed pairs in w) with scale byte sb.
+// half: 0 = each word's low element only, 1 = high only, 2 = both (32 values
+// from 16 words). Writes 8 words of codes.
+__device__ __forceinline__ void codes_of(const uint32_t* w, uint32_t sb, uint32_t* out) {
+  if (sb == 0xFFu) {
 #pragma unroll
-  for (int z = 0; z < 4; ++z) {
-    float2 f = __bfloat1622float2(h[z]);
-    v[2 * z] = f.x;
-    v[2 * z + 1] = f.y;
+    for (int i = 0; i < 8; ++i) out[i] = 0x7F7F7F7Fu;
+    return;
+  }
+  const float inv = mx_inv_scale(sb);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t a = w[2 * i], b = w[2 * i + 1];
+    const uint32_t lo = cvt_e4m3x2(__uint_as_float(a << 16) * inv, __uint_as_float(a & 0xFFFF0000u) * inv);
+    const uint32_t hi = cvt_e4m3x2(__uint_as_float(b << 16) * inv, __uint_as_float(b & 0xFFFF0000u) * inv);
+    out[i] = lo | (hi << 16);
   }
 }
 
-// One CTA works through tiles of 32 rows x 128 columns (grid-stride). Each
-// thread loads the next tile's 64 bytes of its row while it quantises the
-// current one, and the gather index is fetched two tiles ahead, so loads
-// stay in flight across the whole loop.
+// Shared-memory tile: 32 rows x 256 bf16 (512 bytes per row); 16-byte chunk
+// j of row r sits at chunk j ^ ((j >> 3) & 7) ^ (4 * ((r >> 4) & 1)), which
+// makes the row pass's 16-byte accesses (8 lanes = 8 blocks of one row per
+// phase) and the column pass's 4-byte reads (16 adjacent words from rows r
+// and r + 16 per warp) conflict-free.
+__device__ __forceinline__ int qchunk(int j, int row) {
+  return j ^ ((j >> 3) & 7) ^ (((row >> 4) & 1) << 2);
+}
+
+// E4M3 codes of 16 bf16 values (8 packed words) with scale byte sb: 4 words.
+__device__ __forceinline__ void codes_of16(const uint32_t* w, uint32_t sb, uint32_t* out) {
+  if (sb == 0xFFu) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = 0x7F7F7F7Fu;
+    return;
+  }
+  const float inv = mx_inv_scale(sb);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t a = w[2 * i], b = w[2 * i + 1];
+    const uint32_t lo = cvt_e4m3x2(__uint_as_float(a << 16) * inv, __uint_as_float(a & 0xFFFF0000u) * inv);
+    const uint32_t hi = cvt_e4m3x2(__uint_as_float(b << 16) * inv, __uint_as_float(b & 0xFFFF0000u) * inv);
+    out[i] = lo | (hi << 16);
+  }
+}
+
+constexpr int kQStages = 4;  // tiles in the shared-memory ring
+constexpr int kQTileWords = kQRows * 128;
+constexpr int kQSmemBytes = kQStages * kQTileWords * 4;
+
+__device__ __forceinline__ void cp_async_16z(uint32_t dst, const void* src, bool valid) {
+  // zero-fills the 16 bytes when !valid (source size 0)
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+// One CTA works through tiles of 32 rows x 256 columns (grid-stride) with a
+// ring of kQStages tiles in shared memory: each thread copies its own 64
+// bytes (row rr, 32-column block b) of the tile kQStages-1 steps ahead with
+// cp.async straight into the swizzled layout, so three tiles are in flight
+// per CTA without holding registers. Row pass: thread (rr, b) quantises its
+// block row-wise. Column pass: thread c owns the word column c (columns 2c
+// and 2c+1) and quantises both 32-row column blocks. Amax is taken on packed
+// bf16 halves with an integer max.
 __global__ void __launch_bounds__(kQThreads)
     mxfp8_quant_kernel(const __nv_bfloat16* __restrict__ in, long long rows, int cols,
                        long long ld, const int32_t* __restrict__ src, int src_div, int dirs,
                        uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
                        uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col) {
-  __shared__ __align__(16) float tile[kQRows * kQStride];
+  extern __shared__ __align__(16) uint32_t qsm[];  // [kQStages][32 rows x 128 words]
   const int tid = threadIdx.x;
-  const int rr = tid >> 2, b = tid & 3;  // row-pass role: row rr, 32-column block b
-  const long long row_tiles = rows / kQRows;
-  const int col_tiles = cols / kQCols;
-  const long long n_tiles = row_tiles * col_tiles;
-  const long long step = gridDim.x;
+  const int rr = tid >> 3, b = tid & 7;  // row pass: row rr, 32-column block b
+  // Tile indices fit in 32 bits (checked on the host); 64-bit division would
+  // cost more than the quantisation itself.
+  const int row_tiles = (int)(rows / kQRows);
+  const int col_tiles = (cols + kQCols - 1) / kQCols;
+  const int n_tiles = row_tiles * col_tiles;
+  const int step = gridDim.x;
+  const int band_tiles = kQBand * col_tiles;
 
   // Tile order: bands of kQBand row tiles (1024 rows); inside a band the
   // tiles run down the rows first, then across the columns. The CTAs in
   // flight then cover a few thousand columns of about a thousand rows, which
   // keeps the row reads, the row-wise writes and the column-wise writes
   // (rows of the transposed output) in long contiguous runs.
-  auto tile_r0 = [&](long long t) -> long long {
-    const long long band = t / (kQBand * (long long)col_tiles);
-    const long long local = t - band * kQBand * (long long)col_tiles;
-    const long long rows_in = min((long long)kQBand, row_tiles - band * kQBand);
-    return (band * kQBand + local % rows_in) * kQRows;
-  };
-  auto tile_c0 = [&](long long t) -> int {
-    const long long band = t / (kQBand * (long long)col_tiles);
-    const long long local = t - band * kQBand * (long long)col_tiles;
-    const long long rows_in = min((long long)kQBand, row_tiles - band * kQBand);
-    return (int)(local / rows_in) * kQCols;
+  auto tile_rc = [&](int t, int& rt, int& ct) {
+    const int band = t / band_tiles;
+    const int local = t - band * band_tiles;
+    const int rows_in = min(kQBand, row_tiles - band * kQBand);
+    const int lr = local / rows_in;
+    ct = lr;
+    rt = band * kQBand + (local - lr * rows_in);
   };
   // Input row of this thread for tile t (-1: a zero row).
-  auto src_row = [&](long long t) -> long long {
-    const long long r = tile_r0(t) + rr;
+  auto src_row = [&](int t) -> long long {
+    int rt, ct;
+    tile_rc(t, rt, ct);
+    const long long r = (long long)rt * kQRows + rr;
     if (!src) return r;
     const int sv = src[r];
     return sv < 0 ? -1 : (long long)(sv / src_div);
   };
-  auto load = [&](long long t, long long in_row, uint4* raw) {
-    const int c0 = tile_c0(t);
-    if (in_row < 0) {
+  // Copy this thread's 64 bytes of tile t (input row in_row) into ring slot s.
+  auto issue = [&](int t, long long in_row, int s) {
+    int rt, ct;
+    tile_rc(t, rt, ct);
+    const int c = ct * kQCols + 32 * b;
+    const bool ok = in_row >= 0 && c < cols;
+    const __nv_bfloat16* g = ok ? in + in_row * ld + c : in;
+    const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(qsm + s * kQTileWords + rr * 128));
 #pragma unroll
-      for (int q = 0; q < 4; ++q) raw[q] = make_uint4(0, 0, 0, 0);
-    } else {
-      const uint4* p = reinterpret_cast<const uint4*>(in + in_row * ld + c0 + 32 * b);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) raw[q] = __ldcs(p + q);
-    }
+    for (int q = 0; q < 4; ++q) cp_async_16z(base + 16 * qchunk(4 * b + q, rr), g + 8 * q, ok);
   };
 
-  long long t = blockIdx.x;
-  uint4 raw[4];
-  long long row_next2 = 0;
-  if (t < n_tiles) {
-    load(t, src_row(t), raw);
-    if (t + step < n_tiles) row_next2 = src_row(t + step);
-  }
-  for (; t < n_tiles; t += step) {
-    const long long r0 = tile_r0(t);
-    const int c0 = tile_c0(t);
-    float v[32];
+  // Prologue: tiles 0 .. kQStages-2 of this CTA, and the row index of the next.
+  const int t0 = blockIdx.x;
+  long long row_ahead = 0;  // input row of the tile kQStages-1 steps ahead
 #pragma unroll
-    for (int q = 0; q < 4; ++q) bf16x8_to_f32(raw[q], v + 8 * q);
-    // Next tile's data (row index fetched one iteration ago) and the row index
-    // of the tile after it.
-    if (t + step < n_tiles) {
-      const long long row_next = row_next2;
-      if (t + 2 * step < n_tiles) row_next2 = src_row(t + 2 * step);
-      load(t + step, row_next, raw);
+  for (int s = 0; s < kQStages - 1; ++s) {
+    const int ts = t0 + s * step;
+    if (ts < n_tiles) issue(ts, src_row(ts), s);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  if ((long long)t0 + (kQStages - 1) * (long long)step < n_tiles)
+    row_ahead = src_row(t0 + (kQStages - 1) * step);
+
+  int slot = 0;
+  for (int t = t0; t < n_tiles; t += step) {
+    // Issue the tile kQStages-1 steps ahead into the slot freed last iteration.
+    const long long ta = (long long)t + (kQStages - 1) * (long long)step;
+    if (ta < n_tiles) {
+      issue((int)ta, row_ahead, (slot + kQStages - 1) % kQStages);
+      if (ta + step < n_tiles) row_ahead = src_row((int)(ta + step));
     }
-    const long long r = r0 + rr;
-    if (dirs & MOE_QUANT_ROWWISE) {
-      uint32_t sb = mx_scale_byte(block_amax(v));
-      uint4 lo, hi;
-      quant32(v, sb, lo, hi);
-      uint4* o = reinterpret_cast<uint4*>(q_row + r * cols + c0 + 32 * b);
-      o[0] = lo;
-      o[1] = hi;
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group %0;" ::"n"(kQStages - 1) : "memory");
+    __syncthreads();  // tile t is complete in slot `slot` for all threads
+    const uint32_t* tile = qsm + slot * kQTileWords;
+    int rt, ct;
+    tile_rc(t, rt, ct);
+    const long long r0 = (long long)rt * kQRows;
+    const int c0 = ct * kQCols;
+    const int ncol = min(kQCols, cols - c0);  // 256, or 128 for a last half tile
+    if ((dirs & MOE_QUANT_ROWWISE) && 32 * b < ncol) {
+      uint32_t w[16];
+      const uint4* row = reinterpret_cast<const uint4*>(tile + rr * 128);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = row[qchunk(4 * b + q, rr)];
+        w[4 * q] = u.x;
+        w[4 * q + 1] = u.y;
+        w[4 * q + 2] = u.z;
+        w[4 * q + 3] = u.w;
+      }
+      const long long r = r0 + rr;
+      const uint32_t sb = scale_of_bf16_amax(amax_bf16x32(w));
+      uint32_t o[8];
+      codes_of(w, sb, o);
+      uint4* dst = reinterpret_cast<uint4*>(q_row + r * cols + c0 + 32 * b);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
       s_row[mx_scale_offset(r, (c0 >> 5) + b, cols)] = (uint8_t)sb;
     }
     if (dirs & MOE_QUANT_COLWISE) {
+      // Lane pair (2c, 2c+1) owns word column c (columns 2c and 2c+1); each
+      // lane of the pair takes 16 of the 32 rows and the pair combines its
+      // maxima with one shuffle.
+      const int c = tid >> 1, half = tid & 1;
+      if (2 * c < ncol) {
+        uint32_t col[16];
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        *reinterpret_cast<float4*>(&tile[rr * kQStride + qtile_col(b, 4 * k)]) =
-            make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-      __syncthreads();
-      const int c = tid, cb = c >> 5, cj = c & 31;
-      float w[32];
+        for (int i = 0; i < 16; ++i) {
+          const int r = 16 * half + i;
+          col[i] = tile[r * 128 + 4 * qchunk(c >> 2, r) + (c & 3)];
+        }
+        uint32_t m = 0;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) w[i] = tile[i * kQStride + qtile_col(cb, cj)];
-      uint32_t sb = mx_scale_byte(block_amax(w));
-      uint4 lo, hi;
-      quant32(w, sb, lo, hi);
-      uint4* o = reinterpret_cast<uint4*>(q_col + (long long)(c0 + c) * rows + r0);
-      o[0] = lo;
-      o[1] = hi;
-      s_col[mx_scale_offset(c0 + c, r0 >> 5, rows)] = (uint8_t)sb;
-      __syncthreads();
+        for (int i = 0; i < 16; ++i) m = __vmaxu2(m, col[i] & 0x7FFF7FFFu);
+        m = __vmaxu2(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        const uint32_t sb0 = scale_of_bf16_amax(m & 0xFFFFu), sb1 = scale_of_bf16_amax(m >> 16);
+        uint32_t lo[8], hi[8], o[4];
+        // repack: column 2c = low halves, column 2c+1 = high halves
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          lo[i] = (col[2 * i] & 0xFFFFu) | (col[2 * i + 1] << 16);
+          hi[i] = (col[2 * i] >> 16) | (col[2 * i + 1] & 0xFFFF0000u);
+        }
+        const long long rb = r0 + 16 * half;
+        codes_of16(lo, sb0, o);
+        *reinterpret_cast<uint4*>(q_col + (long long)(c0 + 2 * c) * rows + rb) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+        codes_of16(hi, sb1, o);
+        *reinterpret_cast<uint4*>(q_col + (long long)(c0 + 2 * c + 1) * rows + rb) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+        if (half == 0) s_col[mx_scale_offset(c0 + 2 * c, r0 >> 5, rows)] = (uint8_t)sb0;
+        else s_col[mx_scale_offset(c0 + 2 * c + 1, r0 >> 5, rows)] = (uint8_t)sb1;
+      }
     }
+    __syncthreads();  // slot is reused by the copies issued next iteration
+    slot = (slot + 1) % kQStages;
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 }  // namespace
@@ -191,9 +253,17 @@ extern "C" int mxfp8_quantize(const void* in, long long rows, int cols, long lon
   if (!in || !aligned16(in)) return MOE_ERR_ARG;
   if ((dirs & MOE_QUANT_ROWWISE) && (!q_row || !s_row || !aligned16(q_row))) return MOE_ERR_ARG;
   if ((dirs & MOE_QUANT_COLWISE) && (!q_col || !s_col || !aligned16(q_col))) return MOE_ERR_ARG;
-  long long tiles = (rows / kQRows) * (cols / kQCols);
-  long long blocks = tiles < 148 * 12 ? tiles : 148 * 12;
-  mxfp8_quant_kernel<<<(unsigned)blocks, kQThreads, 0, (cudaStream_t)stream>>>(
+  long long tiles = (rows / kQRows) * ((cols + kQCols - 1) / kQCols);
+  if (tiles >= (1LL << 31) - 148LL * 3 * 4) return MOE_ERR_UNSUPPORTED;
+  long long blocks = tiles < 148 * 3 ? tiles : 148 * 3;  // 3 CTAs (192 KB of ring) per SM
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(mxfp8_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kQSmemBytes) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set = true;
+  }
+  mxfp8_quant_kernel<<<(unsigned)blocks, kQThreads, kQSmemBytes, (cudaStream_t)stream>>>(
       static_cast<const __nv_bfloat16*>(in), rows, cols, ld, src, src_div, dirs, q_row, s_row,
       q_col, s_col);
   return launch_status();
