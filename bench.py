@@ -463,8 +463,9 @@ def run_ours(args, wl, world, rank, local):
     clk = clocks.stop()
     ms = t0.elapsed_time(t1)
     ms = max_over_ranks(ms, world)
-    per_kernel = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1])
-                                     for i in range(args.steps))
+    # median over the steps: the first op of the first step also waits for the host
+    per_kernel = {n: statistics.median(evs[i][j].elapsed_time(evs[i][j + 1])
+                                       for i in range(args.steps))
                   for j, n in enumerate(step.NAMES)}
     if B.device_error() != 0:
         raise RuntimeError("device error flag set during the timed region")
@@ -570,7 +571,73 @@ def run_ours(args, wl, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def library_peaks(seconds=3.0):
+    """Dense GEMM throughput of the vendor libraries on this GPU, for the tensor rooflines:
+    cuBLAS BF16 (torch.mm) and cuBLASLt MXFP8 (torch._scaled_mm with 1x32 E8M0 block scales),
+    each as a burst (median of 20 timed calls) and sustained (back-to-back calls for `seconds`,
+    last half). Shapes: 8192^3 and the Mixtral FC1 GEMM (M = 32768 routed rows, K = 4096,
+    N = 28672)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = torch.Generator(device=dev).manual_seed(1)
+    res = {"gpu": torch.cuda.get_device_name(dev), "shapes": {}}
+    for name, (M, K, N) in {"square_8192": (8192, 8192, 8192),
+                            "mixtral_fc1": (32768, 4096, 28672)}.items():
+        flop = 2.0 * M * N * K
+        a16 = torch.randn((M, K), device=dev, generator=g).to(torch.bfloat16)
+        b16 = torch.randn((N, K), device=dev, generator=g).to(torch.bfloat16)
+        a8, b8 = a16.to(torch.float8_e4m3fn), b16.to(torch.float8_e4m3fn)
+        sa = torch.full((128 * -(-M // 128) * 4 * -(-K // 128),), 127, dtype=torch.uint8,
+                        device=dev).view(torch.float8_e8m0fnu)
+        sb = torch.full((128 * -(-N // 128) * 4 * -(-K // 128),), 127, dtype=torch.uint8,
+                        device=dev).view(torch.float8_e8m0fnu)
+        fns = {"bf16": lambda: torch.mm(a16, b16.t()),
+               "mxfp8": lambda: torch._scaled_mm(a8, b8.t(), sa, sb, out_dtype=torch.bfloat16)}
+        out = {}
+        for kind, fn in fns.items():
+            time.sleep(5.0)  # let clocks recover from the previous loop before the burst
+            clk = ClockSampler(0)
+            clk.start()
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(20):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            burst = flop / (sorted(ts)[len(ts) // 2] / 1e3) / 1e12
+            burst_clk = clk.stop()
+            clk = ClockSampler(0)
+            clk.start()
+            per = sorted(ts)[len(ts) // 2] / 1e3
+            n = max(4, int(seconds / per))
+            marks = []
+            for i in range(n):
+                if i in (n // 2, n - 1):
+                    ev = torch.cuda.Event(enable_timing=True)
+                    ev.record()
+                    marks.append(ev)
+                fn()
+            torch.cuda.synchronize()
+            sus_ms = marks[0].elapsed_time(marks[1]) / (n - 1 - n // 2)
+            out[kind] = {"burst_tflops": round(burst, 1), "burst_clocks": burst_clk,
+                         "sustained_tflops": round(flop / (sus_ms / 1e3) / 1e12, 1),
+                         "sustained_clocks": clk.stop()}
+        res["shapes"][name] = out
+        del a16, b16, a8, b8, sa, sb
+        torch.cuda.empty_cache()
+    print(json.dumps(res))
+
+
 def main():
+    if "--library-peaks" in sys.argv:
+        library_peaks()
+        return
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
