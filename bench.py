@@ -110,7 +110,8 @@ class Step:
         self.B = B
         self.wl = wl
         self.router = router
-        self.mx = wl.precision == "mxfp8"
+        self.mx = wl.precision in ("mxfp8", "mxfp8_act4")
+        self.act4 = wl.precision == "mxfp8_act4"
         self.layer = MoELayer(wl.T, wl.H, wl.F, wl.E, wl.k, precision=wl.precision,
                               align=wl.align, device=dev)
         L = self.layer
@@ -183,11 +184,22 @@ class Step:
         else:
             def q(name):
                 return [p(P[f"{name}_{t}"]) for t in ("q_row", "s_row", "q_col", "s_col")]
+
+            def to_fp4(name, cols):  # row-wise MXFP8 -> the MXFP4 copy carried to the backward
+                return lambda: L.mxfp4_from_mxfp8(p(P[f"{name}_q_row"]), p(P[f"{name}_s_row"]),
+                                                  R, cols, p(P[f"{name}4_q_row"]),
+                                                  p(P[f"{name}4_s_row"]), s)
+
+            def col_from_fp4(name, cols):  # the wgrad operand rebuilt from the MXFP4 copy
+                return lambda: L.mxfp8_colwise_from_mxfp4_rowwise(
+                    p(P[f"{name}4_q_row"]), p(P[f"{name}4_s_row"]), R, cols,
+                    p(P[f"{name}_q_col"]), p(P[f"{name}_s_col"]), s)
+            xdirs = B.QUANT_ROWWISE if self.act4 else RC
             ops += [
                 ("p_rows", lambda: L.moe_permute(
                     p(x), p(P["dest"]), p(P["offsets"]), p(P["counts"]), p(P["w"]), T, H, E, k,
                     None, p(P["p_rows"]), s)),
-                ("quant_x", lambda: L.mxfp8_quantize(p(x), R, H, H, p(P["src"]), k, RC,
+                ("quant_x", lambda: L.mxfp8_quantize(p(x), R, H, H, p(P["src"]), k, xdirs,
                                                      *q("x"), s)),
                 ("quant_w1", lambda: L.mxfp8_quantize(p(w1), E * H, 2 * F, 2 * F, None, 1, RC,
                                                       *q("w1"), s)),
@@ -196,6 +208,10 @@ class Step:
                 ("fc1_swiglu", lambda: L.moe_fc1_swiglu_mxfp8(
                     p(P["x_q_row"]), p(P["x_s_row"]), R, H, p(P["w1_q_col"]), p(P["w1_s_col"]),
                     p(P["offsets"]), p(P["p_rows"]), E, F, p(P["gu"]), *q("h"), s)),
+            ]
+            if self.act4:
+                ops += [("x_to_fp4", to_fp4("x", H)), ("h_to_fp4", to_fp4("h", F))]
+            ops += [
                 ("fc2", lambda: L.moe_grouped_gemm_mxfp8(
                     0, p(P["h_q_row"]), p(P["h_s_row"]), R, F, p(P["w2_q_col"]),
                     p(P["w2_s_col"]), H, E * F, 0, F, p(P["offsets"]), E, 0, H, F, p(P["y2"]),
@@ -208,6 +224,11 @@ class Step:
                     p(P["dy2_q_row"]), p(P["dy2_s_row"]), R, H, p(P["w2_q_row"]),
                     p(P["w2_s_row"]), p(P["offsets"]), p(P["p_rows"]), p(P["gu"]), E, F,
                     *q("dy1"), p(P["dp"]), s)),
+            ]
+            if self.act4:
+                ops += [("h_col_from_fp4", col_from_fp4("h", F)),
+                        ("x_col_from_fp4", col_from_fp4("x", H))]
+            ops += [
                 ("fc2_wgrad", lambda: L.moe_grouped_gemm_mxfp8(
                     1, p(P["h_q_col"]), p(P["h_s_col"]), F, R, p(P["dy2_q_col"]),
                     p(P["dy2_s_col"]), H, R, 0, 0, p(P["offsets"]), E, F, H, 0, p(dw2), s)),
@@ -253,6 +274,8 @@ def kernel_work(wl):
     T, H, F, E, k = wl.T, wl.H, wl.F, wl.E, wl.k
     R = T * k
     q2 = 2 * (1 + 1 / 32)  # bytes written per element by a two-direction MXFP8 quantisation
+    q8, q4 = 1 + 1 / 32, 0.5 + 1 / 32  # bytes per element of one MXFP8 / MXFP4 copy
+    act4 = wl.precision == "mxfp8_act4"
     return {
         "fc1_swiglu": ("flops", 4.0 * R * H * F),
         "fc2": ("flops", 2.0 * R * H * F),
@@ -264,7 +287,12 @@ def kernel_work(wl):
         "plan": ("bytes", R * 4.0 * 3),
         "permute_x": ("bytes", T * H * 2.0 + R * H * 2.0),
         "p_rows": ("bytes", R * 4.0 * 3),
-        "quant_x": ("bytes", T * H * 2.0 + R * H * q2),
+        "quant_x": ("bytes", T * H * 2.0 + R * H * (q8 if act4 else q2)),
+        # MXFP4 activation mode: FP8 -> FP4 copies and the rebuilt column-wise FP8
+        "x_to_fp4": ("bytes", R * H * (q8 + q4)),
+        "h_to_fp4": ("bytes", R * F * (q8 + q4)),
+        "x_col_from_fp4": ("bytes", R * H * (q4 + q8)),
+        "h_col_from_fp4": ("bytes", R * F * (q4 + q8)),
         "quant_w1": ("bytes", E * H * 2.0 * F * (2.0 + q2)),
         "quant_w2": ("bytes", E * F * H * (2.0 + q2)),
         "quant_dout": ("bytes", T * H * 2.0 + R * H * q2),
@@ -300,7 +328,7 @@ def oracle_sample_time(wl, t_slice):
     before the clock starts). Returns (seconds, tokens)."""
     from oracle import moe_oracle as O
     x, lg, w1, w2, dout = _oracle_inputs(wl, t_slice)
-    mx = wl.precision == "mxfp8"
+    mx = {"bf16": False, "mxfp8": True, "mxfp8_act4": "act4"}[wl.precision]
     t0 = time.perf_counter()
     chk = 0.0
     for e, tok, slot, y2, dxp, dp, dW1e, dW2e in O.layer_fwd_bwd_expert_stream(
@@ -517,7 +545,7 @@ def run_ours(args, wl, world, rank, local):
     gemm_tflops = wl.gemm_flops_fwd_bwd() / (gemm_ms / 1000.0) / 1e12
     dom = max(per_kernel, key=lambda n: per_kernel[n])
     kind, amount = work[dom]
-    mx = wl.precision == "mxfp8"
+    mx = wl.precision in ("mxfp8", "mxfp8_act4")
     # Tensor peak for the GEMMs' own dtype: the measured sustained bf16 rate
     # (kernels timed inside a long step), times the nominal dense MXFP8/BF16
     # ratio 4.5/2.25 = 2 for the MXFP8 path.
@@ -546,7 +574,8 @@ def run_ours(args, wl, world, rank, local):
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 (mxfp8)" if mx else "bf16",
+        "dtype": ("e4m3 (mxfp8); x, h carried as e2m1 (mxfp4)" if wl.precision == "mxfp8_act4"
+                  else "e4m3 (mxfp8)" if mx else "bf16"),
         "data": "synthetic (seeded, generated on the device)",
         "config": dict(config_of(wl), router=("router projection x W_r, top-k, aux "
                                               "load-balancing loss and their backward included"

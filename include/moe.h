@@ -248,6 +248,47 @@ MOE_API int mxfp8_quantize(const void* in, long long rows, int cols, long long l
                    uint8_t* s_col, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * MXFP4 activation compression (the hgpu.org abstract on MXFP4 training of
+ * MoE models on Hopper: activations are kept in MXFP4 while the GEMMs run in
+ * FP8; FP8 goes to FP4 and back without a BF16 round trip, and the
+ * column-wise copy is derived from the row-wise one with new block scales).
+ *
+ * MXFP4 (OCP Microscaling v1.0): 32-element blocks, E8M0 scale byte
+ * e + 127 with e = clamp(floor(log2(max|v|)) - 2, -127, 127) (all-zero
+ * block: -127); E2M1 codes (sign bit 3; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6
+ * for codes 0..7) = the nearest magnitude to |v| * 2^-e, ties to the even
+ * code, saturating at 6; the sign is kept for zeros. A block holding Inf or
+ * NaN gets scale 0xFF and codes 0. Two codes per byte, element 2i in the low
+ * nibble: data [MN, K] is stored as [MN, K/2] bytes. Scales use the 512-byte
+ * tiled layout of mxfp8_quantize (MN rows, K columns).
+ *
+ * Each conversion decodes its input exactly and applies the output format's
+ * rule, so its result equals quantising the decoded values. Matrices are
+ * [rows, cols] with row-wise blocks along cols; rows % 128 == 0,
+ * cols % 128 == 0; data pointers 16-byte aligned. The caller owns every
+ * buffer; nothing is allocated. MOE_ERR_ARG on a bad argument.
+ *
+ * mxfp4_from_mxfp8: row-wise MXFP8 (q8 [rows, cols] e4m3, s8) -> row-wise
+ *   MXFP4 (q4 [rows, cols/2], s4) over the same blocks.
+ * mxfp8_from_mxfp4: row-wise MXFP4 -> row-wise MXFP8 by the mxfp8_quantize
+ *   rule (lossless: every MXFP4 value is an MXFP8 value).
+ * mxfp4_rowwise_to_colwise: row-wise MXFP4 -> column-wise MXFP4 stored
+ *   transposed (q4c [cols, rows/2], s4c tiled with MN = cols, K = rows):
+ *   blocks of 32 rows, scales computed from the decoded values.
+ * mxfp8_colwise_from_mxfp4_rowwise: the column-wise MXFP4 of the previous
+ *   call, de-quantised to column-wise MXFP8 (q8c [cols, rows], s8c tiled
+ *   with MN = cols, K = rows): the operand layout of an MXFP8 wgrad GEMM. */
+MOE_API int mxfp4_from_mxfp8(const uint8_t* q8, const uint8_t* s8, long long rows, int cols,
+                             uint8_t* q4, uint8_t* s4, moe_stream_t stream);
+MOE_API int mxfp8_from_mxfp4(const uint8_t* q4, const uint8_t* s4, long long rows, int cols,
+                             uint8_t* q8, uint8_t* s8, moe_stream_t stream);
+MOE_API int mxfp4_rowwise_to_colwise(const uint8_t* q4, const uint8_t* s4, long long rows,
+                                     int cols, uint8_t* q4c, uint8_t* s4c, moe_stream_t stream);
+MOE_API int mxfp8_colwise_from_mxfp4_rowwise(const uint8_t* q4, const uint8_t* s4,
+                                             long long rows, int cols, uint8_t* q8c,
+                                             uint8_t* s8c, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Grouped GEMM on tcgen05 tensor cores: one launch for all experts, each with
  * its own weights and its own number of rows ("Efficient MoE Training ...",
  * §Challenge 1: GroupedLinear takes per-expert token counts, split_sizes, and
@@ -391,6 +432,16 @@ MOE_API int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t* s
  *     32-blocks run along its reduction dimension (row-wise for forward and
  *     dgrad, column-wise within an expert group for wgrad). [g|u] is kept in
  *     bf16 for the SwiGLU backward.
+ *   MOE_PRECISION_MXFP8_ACT4 (the hgpu.org abstract on MXFP4 MoE training on
+ *     Hopper: FP8 compute, activations kept in MXFP4): as MXFP8, except the
+ *     two activations that the weight gradients need, X (gathered) and H,
+ *     are carried from the forward to the backward only as row-wise MXFP4
+ *     (parts MOE_PART_X4Q_ROW, MOE_PART_H4Q_ROW: half the bytes of one FP8
+ *     copy), made directly from their row-wise MXFP8 copies
+ *     (mxfp4_from_mxfp8). The backward rebuilds their column-wise MXFP8
+ *     operands with mxfp8_colwise_from_mxfp4_rowwise before the two wgrad
+ *     GEMMs, so dW1 and dW2 see X and H quantised FP8 -> FP4 -> column-wise
+ *     FP4; the column-wise FP8 parts of X and H serve as scratch.
  * Requirements: H % 128 == 0 (H % 256 == 0 for MXFP8), F % 128 == 0,
  * 1 <= k <= 8, k <= E <= 256, align a multiple of 128 (groups are padded with
  * zero rows). moe_layer_workspace_size returns 0 for an unsupported cfg. The
@@ -404,6 +455,7 @@ MOE_API int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t* s
  */
 #define MOE_PRECISION_BF16 0
 #define MOE_PRECISION_MXFP8 1
+#define MOE_PRECISION_MXFP8_ACT4 2
 typedef struct moe_layer_config {
   int T, H, F, E, k;
   int align;
@@ -432,6 +484,8 @@ typedef struct moe_layer_config {
 #define MOE_PART_DY2Q_ROW 32 /* MXFP8 dOut gathered: [R_max, H] (+ 33, 34, 35) */
 #define MOE_PART_DY1Q_ROW 36 /* MXFP8 dY1: [R_max, 2F] (+ 37, 38, 39) */
 #define MOE_PART_DY1S_COL 39
+#define MOE_PART_X4Q_ROW 40 /* MXFP8_ACT4: MXFP4 x gathered [R_max, H/2] bytes (+ 41: scales) */
+#define MOE_PART_H4Q_ROW 42 /* MXFP8_ACT4: MXFP4 H [R_max, F/2] bytes (+ 43: scales) */
 
 MOE_API size_t moe_layer_workspace_size(const moe_layer_config* cfg);
 MOE_API int moe_layer_workspace_part(const moe_layer_config* cfg, int part, size_t* offset,

@@ -37,6 +37,10 @@ SIGNATURES = {
     "moe_permute": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _p, _p, _p]),
     "moe_unpermute": (_i, [_p, _p, _p, _i, _i, _i, _p, _p]),
     "mxfp8_quantize": (_i, [_p, _ll, _i, _ll, _p, _i, _i, _p, _p, _p, _p, _p]),
+    "mxfp4_from_mxfp8": (_i, [_p, _p, _ll, _i, _p, _p, _p]),
+    "mxfp8_from_mxfp4": (_i, [_p, _p, _ll, _i, _p, _p, _p]),
+    "mxfp4_rowwise_to_colwise": (_i, [_p, _p, _ll, _i, _p, _p, _p]),
+    "mxfp8_colwise_from_mxfp4_rowwise": (_i, [_p, _p, _ll, _i, _p, _p, _p]),
     "moe_grouped_gemm_bf16": (_i, [_i, _p, _p, _i, _p, _i, _ll, _i, _i, _i, _p, _p]),
     "moe_fc1_swiglu_bf16": (_i, [_p, _p, _p, _p, _i, _ll, _i, _i, _p, _p, _p]),
     "moe_swiglu_bwd_parts": (_i, [_i]),
@@ -277,6 +281,60 @@ def mxfp8_quantize(x, dirs=QUANT_ROWWISE | QUANT_COLWISE, rows=None, src=None, s
     return out
 
 
+# ------------------------------------------------------------------ MXFP4
+
+def _u8(shape, dev):
+    return torch.empty(shape, dtype=torch.uint8, device=dev)
+
+
+def mxfp4_from_mxfp8(q8, s8, stream=None, out=None):
+    """Row-wise MXFP8 (q8 [rows, cols] bytes, s8 tiled) -> row-wise MXFP4:
+    {"q4": [rows, cols/2] bytes, "s4": tiled scales}."""
+    rows, cols = q8.shape
+    out = out or {"q4": _u8((rows, cols // 2), q8.device),
+                  "s4": _u8(mx_scale_bytes(rows, cols), q8.device)}
+    _check(lib().mxfp4_from_mxfp8(ptr(q8), ptr(s8), rows, cols, ptr(out["q4"]), ptr(out["s4"]),
+                                  stream_handle(stream)), "mxfp4_from_mxfp8")
+    return out
+
+
+def mxfp8_from_mxfp4(q4, s4, stream=None, out=None):
+    """Row-wise MXFP4 (q4 [rows, cols/2]) -> row-wise MXFP8 {"q8", "s8"}."""
+    rows, half = q4.shape
+    cols = 2 * half
+    out = out or {"q8": _u8((rows, cols), q4.device),
+                  "s8": _u8(mx_scale_bytes(rows, cols), q4.device)}
+    _check(lib().mxfp8_from_mxfp4(ptr(q4), ptr(s4), rows, cols, ptr(out["q8"]), ptr(out["s8"]),
+                                  stream_handle(stream)), "mxfp8_from_mxfp4")
+    return out
+
+
+def mxfp4_rowwise_to_colwise(q4, s4, stream=None, out=None):
+    """Row-wise MXFP4 [rows, cols] -> column-wise MXFP4 stored transposed:
+    {"q4c": [cols, rows/2] bytes, "s4c": tiled with MN = cols, K = rows}."""
+    rows, half = q4.shape
+    cols = 2 * half
+    out = out or {"q4c": _u8((cols, rows // 2), q4.device),
+                  "s4c": _u8(mx_scale_bytes(cols, rows), q4.device)}
+    _check(lib().mxfp4_rowwise_to_colwise(ptr(q4), ptr(s4), rows, cols, ptr(out["q4c"]),
+                                          ptr(out["s4c"]), stream_handle(stream)),
+           "mxfp4_rowwise_to_colwise")
+    return out
+
+
+def mxfp8_colwise_from_mxfp4_rowwise(q4, s4, stream=None, out=None):
+    """Row-wise MXFP4 [rows, cols] -> column-wise MXFP8 stored transposed:
+    {"q8c": [cols, rows] bytes, "s8c": tiled with MN = cols, K = rows}."""
+    rows, half = q4.shape
+    cols = 2 * half
+    out = out or {"q8c": _u8((cols, rows), q4.device),
+                  "s8c": _u8(mx_scale_bytes(cols, rows), q4.device)}
+    _check(lib().mxfp8_colwise_from_mxfp4_rowwise(ptr(q4), ptr(s4), rows, cols, ptr(out["q8c"]),
+                                                  ptr(out["s8c"]), stream_handle(stream)),
+           "mxfp8_colwise_from_mxfp4_rowwise")
+    return out
+
+
 # ----------------------------------------------------------- grouped GEMM
 
 def moe_grouped_gemm_bf16(mode, A, B, offsets, b_layout=0, M=0, N=0, K=0, C=None, stream=None):
@@ -385,7 +443,7 @@ def moe_fc2_dgrad_swiglu_bwd_mxfp8(dy2q, sdy2, w2q, sw2, offsets, p_rows, gu, F,
 
 # ------------------------------------------------------------- whole layer
 
-PRECISION = {"bf16": 0, "mxfp8": 1}
+PRECISION = {"bf16": 0, "mxfp8": 1, "mxfp8_act4": 2}
 PARTS = {"idx": (0, torch.int32), "w": (1, torch.float32), "counts": (2, torch.int32),
          "offsets": (3, torch.int32), "dest": (4, torch.int32), "src": (5, torch.int32),
          "p_rows": (7, torch.float32), "xp": (8, torch.bfloat16), "gu": (9, torch.bfloat16),
@@ -395,6 +453,9 @@ PARTS = {"idx": (0, torch.int32), "w": (1, torch.float32), "counts": (2, torch.i
 for _i, _name in enumerate(("x", "w1", "w2", "h", "dy2", "dy1")):
     for _j, _suffix in enumerate(("q_row", "s_row", "q_col", "s_col")):
         PARTS[f"{_name}_{_suffix}"] = (16 + 4 * _i + _j, torch.uint8)
+# MXFP8_ACT4 parts: the row-wise MXFP4 copies of x (gathered) and H
+PARTS.update({"x4_q_row": (40, torch.uint8), "x4_s_row": (41, torch.uint8),
+              "h4_q_row": (42, torch.uint8), "h4_s_row": (43, torch.uint8)})
 
 
 class LayerConfig(C.Structure):

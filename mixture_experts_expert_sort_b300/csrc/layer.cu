@@ -31,10 +31,13 @@ enum Part {
   P_HQ_ROW, P_HS_ROW, P_HQ_COL, P_HS_COL,
   P_DY2Q_ROW, P_DY2S_ROW, P_DY2Q_COL, P_DY2S_COL,
   P_DY1Q_ROW, P_DY1S_ROW, P_DY1Q_COL, P_DY1S_COL,
+  // MXFP8_ACT4 mode only: the row-wise MXFP4 copies of x (gathered) and H.
+  P_X4Q, P_X4S, P_H4Q, P_H4S,
   P_COUNT
 };
 static_assert(P_XQ_ROW == MOE_PART_XQ_ROW && P_W1Q_ROW == MOE_PART_W1Q_ROW &&
-                  P_HQ_ROW == MOE_PART_HQ_ROW && P_DY1S_COL == MOE_PART_DY1S_COL,
+                  P_HQ_ROW == MOE_PART_HQ_ROW && P_DY1S_COL == MOE_PART_DY1S_COL &&
+                  P_X4Q == MOE_PART_X4Q_ROW && P_H4Q == MOE_PART_H4Q_ROW,
               "part ids match include/moe.h");
 
 struct Layout {
@@ -47,7 +50,10 @@ struct Layout {
 
 static size_t up256(size_t b) { return (b + 255) / 256 * 256; }
 
-static bool is_mx(const moe_layer_config* c) { return c->precision == MOE_PRECISION_MXFP8; }
+static bool is_mx(const moe_layer_config* c) {
+  return c->precision == MOE_PRECISION_MXFP8 || c->precision == MOE_PRECISION_MXFP8_ACT4;
+}
+static bool is_act4(const moe_layer_config* c) { return c->precision == MOE_PRECISION_MXFP8_ACT4; }
 
 static bool config_ok(const moe_layer_config* c) {
   if (!c) return false;
@@ -55,7 +61,7 @@ static bool config_ok(const moe_layer_config* c) {
       c->E > 256 || c->k < 1 || c->k > 8 || c->k > c->E)
     return false;
   if (c->align < 128 || c->align % 128 || c->align > 4096) return false;
-  if (c->precision != MOE_PRECISION_BF16 && c->precision != MOE_PRECISION_MXFP8) return false;
+  if (c->precision != MOE_PRECISION_BF16 && !is_mx(c)) return false;
   // MXFP8 wgrad tiles are 256 output columns wide: FC2's wgrad has N = H.
   if (is_mx(c) && c->H % 256) return false;
   long long rmax = (long long)c->T * c->k + (long long)c->E * (c->align - 1);
@@ -104,6 +110,11 @@ static Layout layout(const moe_layer_config* c) {
     L.bytes[mxfirst[i] + 2] = q * m * n;
     L.bytes[mxfirst[i] + 3] = q * mx_scale_bytes(n, m);
   }
+  const size_t a4 = is_act4(c) ? 1 : 0;
+  L.bytes[P_X4Q] = a4 * R * H / 2;
+  L.bytes[P_X4S] = a4 * mx_scale_bytes(R, H);
+  L.bytes[P_H4Q] = a4 * R * F / 2;
+  L.bytes[P_H4S] = a4 * mx_scale_bytes(R, F);
   size_t o = 0;
   for (int i = 0; i < P_COUNT; ++i) {
     L.off[i] = o;
@@ -162,8 +173,12 @@ extern "C" int moe_layer_forward(const moe_layer_config* cfg, const float* logit
     const long long R = L.rmax;
     // per-row routing weights only; the gather of x is fused into its quantisation
     MOE_TRY(moe_permute(x, dest, offsets, counts, w, T, H, E, k, nullptr, p_rows, stream));
-    MOE_TRY(mxfp8_quantize(x, R, H, H, src, k, MOE_QUANT_ROWWISE | MOE_QUANT_COLWISE,
+    // ACT4: the column-wise copy of x is rebuilt from MXFP4 in the backward
+    MOE_TRY(mxfp8_quantize(x, R, H, H, src, k,
+                           is_act4(cfg) ? MOE_QUANT_ROWWISE : MOE_QUANT_ROWWISE | MOE_QUANT_COLWISE,
                            P(P_XQ_ROW), P(P_XS_ROW), P(P_XQ_COL), P(P_XS_COL), stream));
+    if (is_act4(cfg))
+      MOE_TRY(mxfp4_from_mxfp8(P(P_XQ_ROW), P(P_XS_ROW), R, H, P(P_X4Q), P(P_X4S), stream));
     MOE_TRY(mxfp8_quantize(w1, (long long)E * H, 2 * F, 2 * F, nullptr, 1,
                            MOE_QUANT_ROWWISE | MOE_QUANT_COLWISE, P(P_W1Q_ROW), P(P_W1S_ROW),
                            P(P_W1Q_COL), P(P_W1S_COL), stream));
@@ -173,6 +188,8 @@ extern "C" int moe_layer_forward(const moe_layer_config* cfg, const float* logit
     MOE_TRY(moe_fc1_swiglu_mxfp8(P(P_XQ_ROW), P(P_XS_ROW), R, H, P(P_W1Q_COL), P(P_W1S_COL),
                                  offsets, p_rows, E, F, P(P_GU), P(P_HQ_ROW), P(P_HS_ROW),
                                  P(P_HQ_COL), P(P_HS_COL), stream));
+    if (is_act4(cfg))  // H is carried to the backward as MXFP4
+      MOE_TRY(mxfp4_from_mxfp8(P(P_HQ_ROW), P(P_HS_ROW), R, F, P(P_H4Q), P(P_H4S), stream));
     // FC2: B_e[n, f] = W2_e[f, n] from the column-wise copy [H, E*F] (blocks along F)
     MOE_TRY(moe_grouped_gemm_mxfp8(MOE_GEMM_FPROP, P(P_HQ_ROW), P(P_HS_ROW), R, F, P(P_W2Q_COL),
                                    P(P_W2S_COL), H, (long long)E * F, 0, F, offsets, E, 0, H, F,
@@ -217,6 +234,13 @@ extern "C" int moe_layer_backward(const moe_layer_config* cfg, const void* dout,
                                            P(P_W2S_ROW), offsets, p_rows, P(P_GU), E, F,
                                            P(P_DY1Q_ROW), P(P_DY1S_ROW), P(P_DY1Q_COL),
                                            P(P_DY1S_COL), dp, stream));
+    // ACT4: the column-wise operands of the two wgrads come from the MXFP4 copies
+    if (is_act4(cfg)) {
+      MOE_TRY(mxfp8_colwise_from_mxfp4_rowwise(P(P_H4Q), P(P_H4S), R, F, P(P_HQ_COL), P(P_HS_COL),
+                                               stream));
+      MOE_TRY(mxfp8_colwise_from_mxfp4_rowwise(P(P_X4Q), P(P_X4S), R, H, P(P_XQ_COL), P(P_XS_COL),
+                                               stream));
+    }
     // dW2_e = H_e^T dY2_e, both column-wise (blocks along the group's rows)
     MOE_TRY(moe_grouped_gemm_mxfp8(MOE_GEMM_WGRAD, P(P_HQ_COL), P(P_HS_COL), F, R, P(P_DY2Q_COL),
                                    P(P_DY2S_COL), H, R, 0, 0, offsets, E, F, H, 0, dw2, stream));

@@ -6,6 +6,7 @@
 #include "permute.cu"
 #include "plan_static.cu"
 #include "quant.cu"
+#include "mxfp4.cu"
 #include "gemm.cu"
 #include "layer.cu"
 #include "gemm_mx.cu"

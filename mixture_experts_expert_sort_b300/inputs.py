@@ -40,7 +40,7 @@ class Workload:
     F: int
     E: int
     k: int
-    precision: str  # "bf16" or "mxfp8"
+    precision: str  # "bf16", "mxfp8" or "mxfp8_act4" (MXFP8 with MXFP4-carried X and H)
     seed: int
     zipf_s: float = 0.0  # > 0: Zipf-skewed per-expert logit bias
     zero_experts: int = 0  # experts forced to receive no token
@@ -64,6 +64,7 @@ WORKLOADS = {
     "tiny": Workload("tiny", 256, 128, 256, 4, 2, "bf16", 1001),
     "mixtral": Workload("mixtral", 8192, 4096, 14336, 8, 2, "bf16", 1002),
     "mixtral_mx": Workload("mixtral_mx", 16384, 4096, 14336, 8, 2, "mxfp8", 1003),
+    "mixtral_mx4": Workload("mixtral_mx4", 16384, 4096, 14336, 8, 2, "mxfp8_act4", 1003),
     "finegrained": Workload("finegrained", 16384, 2048, 1408, 64, 6, "mxfp8", 1004,
                             zipf_s=1.2, zero_experts=4),
     "long": Workload("long", 65536, 4096, 14336, 8, 2, "mxfp8", 1005, outlier_frac=0.01),

@@ -353,6 +353,29 @@ def mx_qdq_cols_in_groups(a):
     return mx_qdq(pad, axis=0)[:n]
 
 
+def act4_cols_in_groups(a):
+    """Column-wise operand values of one expert group's rows in the MXFP4
+    activation mode [MXFP4-HOPPER]: the rows are quantised row-wise to MXFP8,
+    converted directly to row-wise MXFP4, then to column-wise MXFP4 (blocks
+    of 32 rows, scales recomputed) and to column-wise MXFP8 (lossless). The
+    group is padded with zero rows to a multiple of 32, as in a 32-aligned
+    permuted buffer. Returns the values of the real rows only."""
+    from oracle import mxfp4_oracle as Q  # that module builds on this one
+    a = np.asarray(a, dtype=f64)
+    n = a.shape[0]
+    pad = np.zeros((roundup(n, MX_BLOCK), a.shape[1]), dtype=f64)
+    pad[:n] = a
+    c4, s4 = Q.mxfp4_from_mxfp8(*mx_quantize(pad, axis=1))
+    cc, sc = Q.mx4_quantize(Q.mx4_dequantize(c4, s4, axis=1), axis=0)
+    return Q.mx4_dequantize(cc, sc, axis=0)[:n]
+
+
+def wgrad_act_cols(a, mx):
+    """The column-wise (wgrad) operand values of an activation: MXFP8
+    column-wise, or the MXFP4 chain when mx == "act4"."""
+    return act4_cols_in_groups(a) if mx == "act4" else mx_qdq_cols_in_groups(a)
+
+
 def to_f32(a):
     return np.asarray(a, dtype=np.float32).astype(f64)
 
@@ -463,9 +486,9 @@ def expert_backward(xe, p, W1e, W2e, dy2, saved, mx=False):
         dy1_32 = to_f32(dy1)
         dy1_row = mx_qdq(dy1_32, axis=1)
         dy1_col = mx_qdq_cols_in_groups(dy1_32)
-        h_col = mx_qdq_cols_in_groups(to_f32(h))
+        h_col = wgrad_act_cols(to_f32(h), mx)
         dy2_col = mx_qdq_cols_in_groups(dy2)
-        x_col = mx_qdq_cols_in_groups(xe)
+        x_col = wgrad_act_cols(xe, mx)
     else:
         dy1_row = dy1_col = dy1
         h_col, dy2_col, x_col = h, dy2, xe
@@ -653,9 +676,9 @@ def sampled_weight_grads(x, logits, W1, W2, dout, k, fcols, mx=False):
         dg = dA * u * dsilu(g)
         du = dA * silu(g)
         if mx:
-            h_col = mx_qdq_cols_in_groups(to_f32(h))
+            h_col = wgrad_act_cols(to_f32(h), mx)
             dy2_col = mx_qdq_cols_in_groups(dy2)
-            x_col = mx_qdq_cols_in_groups(xe)
+            x_col = wgrad_act_cols(xe, mx)
             dg_col = mx_qdq_cols_in_groups(to_f32(dg))
             du_col = mx_qdq_cols_in_groups(to_f32(du))
         else:

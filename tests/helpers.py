@@ -26,6 +26,12 @@ def scales_tiled_to_rowmajor(s, mn, kdim):
     return s.transpose(0, 3, 2, 1, 4).reshape(mn, kdim // 32)
 
 
+def scales_rowmajor_to_tiled(s, mn, kdim):
+    """Inverse of scales_tiled_to_rowmajor: [mn, kdim/32] to the tiled bytes."""
+    s = np.asarray(s, dtype=np.uint8).reshape(mn // 128, 4, 32, kdim // 128, 4)
+    return np.ascontiguousarray(s.transpose(0, 3, 2, 1, 4)).reshape(-1)
+
+
 def rel_fro(a, ref):
     a = np.asarray(a, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)

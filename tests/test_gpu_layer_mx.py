@@ -23,10 +23,10 @@ DEV = "cuda"
 TOL_MX = 1e-2
 
 
-def _run(wl, inp):
+def _run(wl, inp, precision="mxfp8"):
     from mixture_experts_expert_sort_b300 import binding
     from mixture_experts_expert_sort_b300.layer import MoELayer
-    L = MoELayer(wl.T, wl.H, wl.F, wl.E, wl.k, precision="mxfp8", align=wl.align)
+    L = MoELayer(wl.T, wl.H, wl.F, wl.E, wl.k, precision=precision, align=wl.align)
     d = {k: v.to(DEV) for k, v in inp.items()}
     out = L.forward(d["logits"], d["x"], d["w1"], d["w2"])
     dx, dw1, dw2, dl = L.backward(d["dout"], d["w1"], d["w2"])
@@ -77,8 +77,9 @@ def _check_colwise(L, name, mn, kd, blocks, block_vals):
         np.testing.assert_array_equal(s[:, b], rs[0], err_msg=f"{name} column-wise scales, {b}")
 
 
-def _check_input_quantisation(L, wl, inp, n_rows=None, n_blocks=None, seed=0):
-    """Bit-exact MXFP8 of the gathered x and dOut and of both weights."""
+def _check_input_quantisation(L, wl, inp, n_rows=None, n_blocks=None, seed=0, act4=False):
+    """Bit-exact MXFP8 of the gathered x and dOut and of both weights (in the
+    MXFP4 activation mode the column-wise x is checked by _check_act4_x)."""
     rng = np.random.default_rng(seed)
     src, R = _rows_of(L, wl)
     k = wl.k
@@ -90,6 +91,8 @@ def _check_input_quantisation(L, wl, inp, n_rows=None, n_blocks=None, seed=0):
         x = t.float().numpy()
         rows = pick(R, n_rows)
         _check_rowwise(L, name, R, wl.H, rows, _gathered(x, src, k, rows))
+        if act4 and name == "x":
+            continue
         blocks = pick(R // 32, n_blocks)
         _check_colwise(L, name, R, wl.H, blocks,
                        [_gathered(x, src, k, np.arange(32 * b, 32 * b + 32)) for b in blocks])
@@ -200,6 +203,50 @@ def _sampled_parity(wl, n_tokens=256):
         assert not torch.any(g["dW1"][int(e)]) and not torch.any(g["dW2"][int(e)])
 
 
+def _check_act4_x(L, wl, inp):
+    """MXFP4 activation mode, bit-exact on the input side: the saved MXFP4 copy
+    of the gathered x (FP8 -> FP4 of its row-wise MXFP8) and the column-wise
+    MXFP8 operand the backward rebuilt from it."""
+    from oracle import mxfp4_oracle as Q
+    src, R = _rows_of(L, wl)
+    xg = _gathered(inp["x"].float().numpy(), src, wl.k, np.arange(R))
+    c4, s4 = Q.mxfp4_from_mxfp8(*O.mx_quantize(xg, axis=1))
+    np.testing.assert_array_equal(u8(L.part("x4_q_row")).reshape(R, wl.H // 2), Q.pack_e2m1(c4))
+    np.testing.assert_array_equal(
+        scales_tiled_to_rowmajor(u8(L.part("x4_s_row")), R, wl.H), s4)
+    c8c, s8c = Q.mxfp8_col_from_mxfp4_row(c4, s4)
+    np.testing.assert_array_equal(u8(L.part("x_q_col")).reshape(wl.H, R), c8c)
+    np.testing.assert_array_equal(
+        scales_tiled_to_rowmajor(u8(L.part("x_s_col")), wl.H, R), s8c)
+
+
+@pytest.mark.parametrize("T,H,F,E,k,zs,ze,of", EDGE[:4] + EDGE[5:])
+def test_act4_layer_full_parity(T, H, F, E, k, zs, ze, of):
+    """MXFP8 compute with X and H carried to the backward as MXFP4: every
+    output against the oracle emulating the same FP8 -> FP4 -> column-wise
+    chain, and the x side byte for byte."""
+    wl = I.Workload("edge_mx4", T, H, F, E, k, "mxfp8", 3100 + T + E, zipf_s=zs,
+                    zero_experts=ze, outlier_frac=of)
+    inp = I.make_all(wl)
+    L, g = _run(wl, inp, precision="mxfp8_act4")
+    x, lg = f64(inp["x"]), f64(inp["logits"])
+    w1, w2, dout = f64(inp["w1"]), f64(inp["w2"]), f64(inp["dout"])
+    fwd = O.layer_forward(x, lg, w1, w2, wl.k, mx="act4")
+    bwd = O.layer_backward(fwd, x, w1, w2, dout)
+    _check_plan(L, wl, fwd["idx"])
+    _check_input_quantisation(L, wl, inp, act4=True)
+    _check_act4_x(L, wl, inp)
+    _check("out", f64(g["out"]), fwd["out"])
+    _check("dX", f64(g["dX"]), bwd["dX"])
+    _check("dW1", f64(g["dW1"]), bwd["dW1"])
+    _check("dW2", f64(g["dW2"]), bwd["dW2"])
+    _check_dlogits(f64(g["dlogits"]), bwd["dlogits"], bwd["dp"], strict=T >= 100)
+    # the MXFP4 chain is what the weight gradients saw: the plain MXFP8
+    # oracle differs from it by more than the tolerance on dW1
+    ref8 = O.layer_backward(O.layer_forward(x, lg, w1, w2, wl.k, mx=True), x, w1, w2, dout)
+    assert rel_fro(bwd["dW1"], ref8["dW1"]) > 2 * rel_fro(f64(g["dW1"]), bwd["dW1"])
+
+
 @pytest.mark.slow
 def test_mixtral_mx_workload_sampled_parity():
     """T=16384, H=4096, F=14336, E=8, top-2, MXFP8."""
@@ -218,3 +265,29 @@ def test_finegrained_workload_sampled_parity():
 def test_long_workload_sampled_parity():
     """T=65536, H=4096, F=14336, E=8, top-2, MXFP8, 1% of x rows scaled x100."""
     _sampled_parity(I.WORKLOADS["long"])
+
+
+@pytest.mark.slow
+def test_mixtral_act4_workload_sampled_parity():
+    """T=16384, H=4096, F=14336, E=8, top-2, MXFP8 compute with MXFP4-carried
+    X and H: sampled tokens and weight-gradient columns against the oracle."""
+    wl = I.WORKLOADS["mixtral_mx"]
+    inp = I.make_all(wl)
+    L, g = _run(wl, inp, precision="mxfp8_act4")
+    x = inp["x"].float().numpy()
+    lg = inp["logits"].numpy()
+    w1 = inp["w1"].float().numpy()
+    w2 = inp["w2"].float().numpy()
+    dout = inp["dout"].float().numpy()
+    rng = np.random.default_rng(wl.seed + 1)
+    toks = np.sort(rng.choice(wl.T, 128, replace=False))
+    s = O.sampled_token_outputs(x, lg, w1, w2, dout, wl.k, toks, mx="act4")
+    _check("out", f64(g["out"])[toks], s["out"])
+    _check("dX", f64(g["dX"])[toks], s["dX"])
+    fb = np.sort(rng.choice(wl.F // 32, 1, replace=False))
+    cols = np.arange(32 * fb[0], 32 * fb[0] + 32)
+    wg = O.sampled_weight_grads(x, lg, w1, w2, dout, wl.k, cols, mx="act4")
+    tc = torch.as_tensor(cols, device=DEV)
+    _check("dW1 gate", f64(g["dW1"][:, :, tc]), wg["dW1g"])
+    _check("dW1 up", f64(g["dW1"][:, :, wl.F + tc]), wg["dW1u"])
+    _check("dW2", f64(g["dW2"][:, tc, :]), wg["dW2"])
