@@ -261,16 +261,19 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------ row -> column
-// CTA: tiles of 128 rows x 64 columns (grid-stride) through a ring of
+// CTA: tiles of 128 rows x 128 columns (grid-stride) through a ring of
 // kRCStages tiles in shared memory, filled by cp.async: the packed codes
-// (128 rows x 32 bytes, one 16-byte chunk per thread) and the 512-byte scale
-// tile that holds the tile's row-block scales (32 threads). Then thread
-// (column c, row block h) decodes rows 32h .. 32h + 31 of column c with their
-// row-block scales, quantises them as one column block and writes 16 (FP4)
-// or 32 (FP8) bytes of the transposed output; the four row blocks of a
-// column write adjacent bytes. A NaN anywhere in a column block makes it NaN.
-constexpr int kRCRows = 128, kRCCols = 64, kRCStages = 4;
-constexpr int kRCTileBytes = kRCRows * (kRCCols / 2) + 512;
+// (128 rows x 64 bytes, two 16-byte chunks per thread) and the 512-byte
+// scale tile holding exactly the tile's row-block scales. Each tile's scales
+// are turned into floats once (NaN for 0xFF); each thread then takes one
+// byte column (columns 2b and 2b + 1) of one 32-row block, decodes the two
+// codes of every byte through a 16-entry table, quantises both columns as
+// column blocks and writes 16 (FP4) or 32 (FP8) bytes of the transposed
+// output for each; the four row blocks of a column write adjacent bytes.
+// About seven instructions per element: the conversion stays memory-bound.
+constexpr int kRCRows = 128, kRCCols = 128, kRCStages = 3;
+constexpr int kRCDataBytes = kRCRows * (kRCCols / 2);
+constexpr int kRCTileBytes = kRCDataBytes + 512;
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
@@ -279,13 +282,63 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
                : "memory");
 }
 
+// 32 values (all finite) -> 16 bytes of E2M1 codes; returns the scale byte.
+__device__ __forceinline__ uint32_t encode_e2m1_col(const float* v, float amax, uint4& out) {
+  const uint32_t s = mx4_scale_byte(amax);
+  const float inv = e8m0_inverse(s);
+  uint32_t w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t b0 = cvt_e2m1x2(v[8 * q] * inv, v[8 * q + 1] * inv);
+    const uint32_t b1 = cvt_e2m1x2(v[8 * q + 2] * inv, v[8 * q + 3] * inv);
+    const uint32_t b2 = cvt_e2m1x2(v[8 * q + 4] * inv, v[8 * q + 5] * inv);
+    const uint32_t b3 = cvt_e2m1x2(v[8 * q + 6] * inv, v[8 * q + 7] * inv);
+    w[q] = __byte_perm(b0 | (b1 << 8), b2 | (b3 << 8), 0x5410);
+  }
+  out = make_uint4(w[0], w[1], w[2], w[3]);
+  return s;
+}
+
 template <bool TO_FP8>
-__global__ void __launch_bounds__(256)
+__device__ __forceinline__ void store_col_block(const float* v, float amax, bool nan,
+                                                uint8_t* __restrict__ qc, uint8_t* __restrict__ sc,
+                                                long long rows, long long col, long long rb) {
+  const long long so = mx_scale_offset(col, rb >> 5, rows);
+  uint4 o4 = make_uint4(0, 0, 0, 0);
+  uint32_t s4out = 0xFFu;
+  if (!nan) s4out = encode_e2m1_col(v, amax, o4);
+  if (!TO_FP8) {
+    __stcs(reinterpret_cast<uint4*>(qc + col * (rows / 2) + (rb >> 1)), o4);
+    sc[so] = (uint8_t)s4out;
+  } else {
+    uint4 o0 = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu), o1 = o0;
+    uint32_t s8out = 0xFFu;
+    if (!nan) {  // the FP4 column block to MXFP8 (lossless)
+      const uint32_t w[4] = {o4.x, o4.y, o4.z, o4.w};
+      Fp8Table tb;
+      s8out = fp8_table(mx4_max_mag(w, 4), s4out, tb);
+      fp8_from_codes8(w[0], tb, o0.x, o0.y);
+      fp8_from_codes8(w[1], tb, o0.z, o0.w);
+      fp8_from_codes8(w[2], tb, o1.x, o1.y);
+      fp8_from_codes8(w[3], tb, o1.z, o1.w);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(qc + col * rows + rb);
+    __stcs(dst, o0);
+    __stcs(dst + 1, o1);
+    sc[so] = (uint8_t)s8out;
+  }
+}
+
+template <bool TO_FP8>
+__global__ void __launch_bounds__(256, 2)
     mxfp4_row_to_col_kernel(const uint8_t* __restrict__ q4, const uint8_t* __restrict__ s4,
                             long long rows, int cols, uint8_t* __restrict__ qc,
                             uint8_t* __restrict__ sc) {
   __shared__ __align__(16) uint8_t ring[kRCStages][kRCTileBytes];
+  __shared__ float sf[kRCRows][4];  // row-block scales of the current tile as floats
+  __shared__ float tab[16];         // E2M1 code -> value
   const int tid = threadIdx.x;
+  if (tid < 16) tab[tid] = e2m1_value((uint32_t)tid);
   const int col_tiles = cols / kRCCols;
   const long long n_tiles = (rows / kRCRows) * col_tiles;
   const long long step = gridDim.x;
@@ -293,67 +346,58 @@ __global__ void __launch_bounds__(256)
     if (t < n_tiles) {
       const long long rt = t / col_tiles;
       const int ct = (int)(t - rt * col_tiles);
-      const long long r = rt * kRCRows + (tid >> 1);
-      cp_async16(&ring[slot][tid * 16], q4 + r * (cols / 2) + ct * (kRCCols / 2) + 16 * (tid & 1));
-      if (tid < 32) {  // the 512-byte scale tile (row tile rt, k tile ct / 2)
-        const long long so = (rt * (cols / 128) + (ct >> 1)) * 512;
-        cp_async16(&ring[slot][kRCRows * (kRCCols / 2) + tid * 16], s4 + so + tid * 16);
+      const uint8_t* src = q4 + rt * kRCRows * (cols / 2) + ct * (kRCCols / 2);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int chunk = tid + 256 * j;  // row chunk >> 2, 16-byte piece chunk & 3
+        cp_async16(&ring[slot][chunk * 16], src + (long long)(chunk >> 2) * (cols / 2) + 16 * (chunk & 3));
       }
+      if (tid < 32)  // the scale tile (row tile rt, k tile ct)
+        cp_async16(&ring[slot][kRCDataBytes + tid * 16], s4 + (rt * col_tiles + ct) * 512 + tid * 16);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
 #pragma unroll
   for (int i = 0; i < kRCStages - 1; ++i) issue(blockIdx.x + i * step, i);
   int slot = 0;
-  const int c = tid & (kRCCols - 1), h = tid >> 6;
+  const int bc = tid & 63, h = tid >> 6;  // byte column (columns 2bc, 2bc+1), row block
   for (long long t = blockIdx.x; t < n_tiles; t += step) {
     issue(t + (kRCStages - 1) * step, (slot + kRCStages - 1) % kRCStages);
     asm volatile("cp.async.wait_group %0;" ::"n"(kRCStages - 1) : "memory");
+    __syncthreads();  // tile t landed (and tab is written)
+    {
+      // scale of (row 32a + b, block c) is byte 16b + 4a + c of the scale tile
+      const uint8_t* st = ring[slot] + kRCDataBytes;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int e = tid + 256 * j;  // e = 16 b + 4 a + c
+        const uint32_t sv = st[e];
+        sf[32 * ((e >> 2) & 3) + (e >> 4)][e & 3] =
+            sv == 0xFFu ? __uint_as_float(0x7FC00000u) : e8m0_value(sv);
+      }
+    }
     __syncthreads();
-    const uint8_t* data = ring[slot];
-    const uint8_t* scl = ring[slot] + kRCRows * (kRCCols / 2);
-    const long long rt = t / col_tiles;
-    const int ct = (int)(t - rt * col_tiles);
-    // scale of (row 32h + i, this column's 32-column block) in the scale tile:
-    // byte 16 i + 4 h + kc, kc = the block's index within its 128 columns
-    const int kc = ((ct & 1) << 1) | (c >> 5);
-    float v[32];
+    const uint8_t* data = ring[slot] + (32 * h) * (kRCCols / 2) + bc;
+    const int blk = bc >> 4;  // 32-column block of columns 2bc, 2bc+1
+    float v0[32], v1[32];
+    float m0 = 0.f, m1 = 0.f;
     bool nan = false;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const uint32_t byte = data[(32 * h + i) * (kRCCols / 2) + (c >> 1)];
-      const uint32_t s = scl[16 * i + 4 * h + kc];
-      const float sv = s == 0xFFu ? __uint_as_float(0x7FC00000u) : e8m0_value(s);
-      v[i] = e2m1_value(byte >> (4 * (c & 1))) * sv;
-      nan |= s == 0xFFu;
+      const uint32_t byte = data[i * (kRCCols / 2)];
+      const float s = sf[32 * h + i][blk];
+      nan |= s != s;
+      v0[i] = tab[byte & 15u] * s;
+      v1[i] = tab[byte >> 4] * s;
+      m0 = fmaxf(m0, fabsf(v0[i]));
+      m1 = fmaxf(m1, fabsf(v1[i]));
     }
-    __syncthreads();  // the slot is refilled by the copy issued next iteration
-    const long long col = (long long)ct * kRCCols + c;
-    const long long rb = rt * kRCRows + 32 * h;  // first row of this column block
-    const long long so = mx_scale_offset(col, rb >> 5, rows);
-    uint4 o4 = make_uint4(0, 0, 0, 0);
-    uint32_t s4out = 0xFFu;
-    if (!nan) s4out = encode_e2m1_block(v, o4);
-    if (!TO_FP8) {
-      __stcs(reinterpret_cast<uint4*>(qc + col * (rows / 2) + (rb >> 1)), o4);
-      sc[so] = (uint8_t)s4out;
-    } else {
-      uint4 o0 = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu), o1 = o0;
-      uint32_t s8out = 0xFFu;
-      if (!nan) {  // the FP4 column block to MXFP8 (lossless)
-        const uint32_t w[4] = {o4.x, o4.y, o4.z, o4.w};
-        Fp8Table tb;
-        s8out = fp8_table(mx4_max_mag(w, 4), s4out, tb);
-        fp8_from_codes8(w[0], tb, o0.x, o0.y);
-        fp8_from_codes8(w[1], tb, o0.z, o0.w);
-        fp8_from_codes8(w[2], tb, o1.x, o1.y);
-        fp8_from_codes8(w[3], tb, o1.z, o1.w);
-      }
-      uint4* dst = reinterpret_cast<uint4*>(qc + col * rows + rb);
-      __stcs(dst, o0);
-      __stcs(dst + 1, o1);
-      sc[so] = (uint8_t)s8out;
-    }
+    __syncthreads();  // the slot and sf are rewritten next iteration
+    const long long rt = t / col_tiles;
+    const long long col = (t - rt * col_tiles) * kRCCols + 2 * bc;
+    const long long rb = rt * kRCRows + 32 * h;  // first row of these column blocks
+    store_col_block<TO_FP8>(v0, m0, nan, qc, sc, rows, col, rb);
+    store_col_block<TO_FP8>(v1, m1, nan, qc, sc, rows, col + 1, rb);
     slot = (slot + 1) % kRCStages;
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -403,7 +447,7 @@ int launch_row_to_col(const uint8_t* q4, const uint8_t* s4, long long rows, int 
   const int rc = check_mx4_args(q4, s4, rows, cols, qc, sc);
   if (rc != MOE_OK) return rc;
   const long long tiles = (rows / kRCRows) * (cols / kRCCols);
-  const unsigned grid = (unsigned)(tiles < 148 * 8 ? tiles : 148 * 8);
+  const unsigned grid = (unsigned)(tiles < 148 * 2 ? tiles : 148 * 2);  // one wave, 2 CTAs per SM
   mxfp4_row_to_col_kernel<TO_FP8><<<grid, 256, 0, (cudaStream_t)stream>>>(q4, s4, rows, cols, qc,
                                                                           sc);
   return launch_status();
