@@ -70,44 +70,6 @@ __device__ __forceinline__ bool e4m3x4_has_nan(uint32_t w) {
   return __vcmpeq4(w & 0x7F7F7F7Fu, 0x7F7F7F7Fu) != 0;
 }
 
-// 32 values of one block (all finite) -> 16 bytes of E2M1 codes and the scale byte.
-__device__ __forceinline__ uint32_t encode_e2m1_block(const float* v, uint4& out) {
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  const uint32_t s = mx4_scale_byte(amax);
-  const float inv = e8m0_inverse(s);
-  uint32_t w[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t x = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      x |= cvt_e2m1x2(v[8 * q + 2 * j] * inv, v[8 * q + 2 * j + 1] * inv) << (8 * j);
-    w[q] = x;
-  }
-  out = make_uint4(w[0], w[1], w[2], w[3]);
-  return s;
-}
-
-// 32 values of one block (all finite) -> 32 bytes of E4M3 codes and the scale byte
-// (the MXFP8 rule of mxfp8_quantize).
-__device__ __forceinline__ uint32_t encode_e4m3_block(const float* v, uint4& o0, uint4& o1) {
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  const uint32_t s = mx_scale_byte(amax);
-  const float inv = mx_inv_scale(s);
-  uint32_t w[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q)
-    w[q] = (uint32_t)cvt_e4m3x2(v[4 * q] * inv, v[4 * q + 1] * inv) |
-           ((uint32_t)cvt_e4m3x2(v[4 * q + 2] * inv, v[4 * q + 3] * inv) << 16);
-  o0 = make_uint4(w[0], w[1], w[2], w[3]);
-  o1 = make_uint4(w[4], w[5], w[6], w[7]);
-  return s;
-}
-
 // ---------------------------------------------- FP4 -> FP8 in integer arithmetic
 // For an MXFP4 block with scale byte s4 whose largest magnitude code is
 // m_max > 0, the largest value is E2M1(m_max) 2^(s4-127) with

@@ -66,16 +66,9 @@ __device__ __forceinline__ uint4 ld_v4(const __nv_bfloat16* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
-// 16-byte cp.async into shared memory, zero-filled when !valid. Each lane
-// later reads back only what it copied itself, so a per-thread
-// cp.async.wait_group is the only synchronisation needed.
-__device__ __forceinline__ void cp16(void* smem, const void* gmem, bool valid) {
-  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d),
-               "l"(reinterpret_cast<uint64_t>(gmem)),
-               "r"(valid ? 16 : 0)
-               : "memory");
-}
+// 16-byte cp.async into shared memory (a shared-window address), zero-filled
+// when !valid. Each lane later reads back only what it copied itself, so a
+// per-thread cp.async.wait_group is the only synchronisation needed.
 __device__ __forceinline__ void cp16s(uint32_t d, const void* gmem, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d),
                "l"(reinterpret_cast<uint64_t>(gmem)), "r"(valid ? 16 : 0)
