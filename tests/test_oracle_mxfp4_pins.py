@@ -155,3 +155,34 @@ def test_fp8_col_from_fp4_row_is_lossless_fp4_col():
     cc, sc = Q.mxfp4_row_to_col(c4, s4)
     np.testing.assert_array_equal(O.mx_dequantize(c8c, s8c, axis=1),
                                   Q.mx4_dequantize(cc, sc, axis=1))
+
+
+def test_act4_chain_exact_on_powers_of_two():
+    """The wgrad operand chain of the MXFP4 activation mode (row-wise MXFP8 ->
+    row-wise MXFP4 -> column-wise MXFP4, groups padded to 32 rows) returns
+    values that every step represents exactly: +-2^(a_r + b_c) spanning three
+    binades in every row block and every column block. 50 rows: the last
+    column block is padded with zero rows."""
+    rng = np.random.default_rng(6)
+    a = rng.integers(0, 2, 50)
+    b = rng.integers(0, 2, 64)
+    x = np.ldexp(1.0, a[:, None] + b[None, :] - 3) * rng.choice([-1.0, 1.0], (50, 64))
+    np.testing.assert_array_equal(O.act4_cols_in_groups(x), x)
+
+
+def test_act4_chain_is_coarser_than_mxfp8():
+    """On random data the chain loses more than column-wise MXFP8 alone (E2M1
+    keeps one mantissa bit against E4M3's three: about 5x the mean error
+    here), and stays within the E2M1 rounding of its two FP4 steps (the
+    row-wise FP8 step is finer than both)."""
+    rng = np.random.default_rng(7)
+    x = rng.normal(size=(96, 64))
+    m8 = np.abs(O.mx_qdq_cols_in_groups(x) - x).mean()
+    m4 = np.abs(O.act4_cols_in_groups(x) - x).mean()
+    assert 3 * m8 < m4 < 8 * m8
+    # per column block: |err| <= 2 * (half the largest E2M1 spacing, 1.0, times the
+    # block scale 2^(floor(log2 amax) - 2)) plus the FP8 step
+    amax = np.abs(x).reshape(3, 32, 64).max(axis=1)
+    scale = np.ldexp(1.0, np.floor(np.log2(amax)).astype(int) - 2)
+    err = np.abs(O.act4_cols_in_groups(x) - x).reshape(3, 32, 64)
+    assert np.all(err <= 2.0 * scale[:, None, :] + 2.0 ** -4 * amax[:, None, :])
