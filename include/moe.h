@@ -67,6 +67,14 @@ MOE_API const char* moe_status_string(int status);
  * Returns MOE_ERR_DEVICE when any bit was set, MOE_OK otherwise. */
 MOE_API int moe_device_error(moe_stream_t stream, unsigned* flags);
 
+/* moe_selftest_wait_timeout: a diagnostic of the failure detection above.
+ * Launches one CTA in which two warps wait, with the bounded wait every
+ * pipelined kernel of this library uses, on an mbarrier that nothing arrives
+ * at. After the library's wait limit (2 s) the wait gives up, sets
+ * MOE_DEVERR_TIMEOUT and the kernel returns; the context stays usable and a
+ * following moe_device_error reports the bit. Nothing else is touched. */
+MOE_API int moe_selftest_wait_timeout(moe_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Routing. "How MoE Architecture Cuts Costs and Boosts Efficiency: Efficient
  * Training of Biological Foundation Models", the Router paragraph (top-K

@@ -28,6 +28,7 @@ _p, _i, _ll, _sz, _u = C.c_void_p, C.c_int, C.c_longlong, C.c_size_t, C.c_uint
 SIGNATURES = {
     "moe_status_string": (C.c_char_p, [_i]),
     "moe_device_error": (_i, [_p, C.POINTER(_u)]),
+    "moe_selftest_wait_timeout": (_i, [_p]),
     "moe_route": (_i, [_p, _i, _i, _i, _p, _p, _p]),
     "moe_route_backward": (_i, [_p, _ll, _i, _p, _p, _p, _i, _i, _i, _p, _p]),
     "moe_rows_padded_max": (_ll, [_i, _i, _i, _i]),
@@ -103,6 +104,12 @@ def device_error(stream=None) -> int:
     if st not in (MOE_OK, MOE_ERR_DEVICE):
         _check(st, "moe_device_error")
     return flags.value
+
+
+def selftest_wait_timeout(stream=None):
+    """Run the library's bounded-wait self-test (about 2 s on the device); the
+    timeout bit then shows in device_error()."""
+    _check(lib().moe_selftest_wait_timeout(stream_handle(stream)), "moe_selftest_wait_timeout")
 
 
 # ----------------------------------------------------------------- routing

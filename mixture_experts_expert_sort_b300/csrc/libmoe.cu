@@ -10,3 +10,4 @@
 #include "gemm.cu"
 #include "layer.cu"
 #include "gemm_mx.cu"
+#include "diag.cu"
