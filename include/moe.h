@@ -111,8 +111,10 @@ MOE_API int moe_route_backward(const float* dp, long long ld_dp, int n_part, con
  * training objective penalises uneven expert load).
  *
  * moe_router_forward:
- *   logits[t, e] = sum_h x[t, h] * w_r[h, e]   (fp32; H is summed in fixed slices
- *                  that are added in order, so the result is deterministic)
+ *   logits[t, e] = sum_h x[t, h] * w_r[h, e]   (exact bf16 products summed in
+ *                  fp32 on warp-level tensor-core MMAs; 128-column chunks of H
+ *                  go to 8 warps whose sums are added in warp order, so the
+ *                  result is deterministic)
  *   idx, w       = moe_route(logits, k)
  *   aux          = [L_aux, f_0..f_{E-1}, P_0..P_{E-1}] (fp32, 1 + 2E values) with
  *                  f_e = #{(t, j): idx[t, j] = e} / (T*k), P_e = mean over t of
@@ -133,6 +135,10 @@ MOE_API int moe_route_backward(const float* dp, long long ld_dp, int n_part, con
  *   dx_out[t, h]  = dx_in[t, h] + sum_e dlogits[t, e] * w_r[h, e]  (bf16;
  *                   dx_in may be NULL or equal dx_out, e.g. the experts' dX),
  *   dw_r[h, e]    = sum_t x[t, h] * dlogits[t, e]  (bf16).
+ *   Both contractions run on warp-level bf16 MMAs with fp32 accumulation;
+ *   dlogits enters them as two bf16 terms, hi = bf16(dl) and
+ *   lo = bf16(dl - hi), about 16 significant bits (the dropped remainder is
+ *   below 2^-16 |dl|). Token sums are taken in a fixed order.
  *   logits and aux as written by moe_router_forward; dlogits [T, E] fp32 (out;
  *   may be the same buffer as dlogits_route). w_r, dx_in and dx_out 16-byte
  *   aligned.

@@ -15,9 +15,10 @@
 //   dL_aux / dlogits[t, e] = (E / T) * s[t, e] * (f_e - sum_i f_i * s[t, i])
 // (f is piecewise constant: the top-k selection carries no gradient.)
 //
-// All kernels are memory-bound SIMT code; every reduction over tokens is done
-// in a fixed order (per-block partials, then one ordered pass), so results do
-// not depend on scheduling.
+// All kernels are memory-bound. The three contractions run on warp-level
+// bf16 MMAs (see "tensor-core tiles" below), the statistics in SIMT code;
+// every reduction is done in a fixed order (per-warp or per-block partials,
+// then one ordered pass), so results do not depend on scheduling.
 #include "common.cuh"
 
 namespace moe {
