@@ -49,7 +49,11 @@ Readings where the sources are silent (each is repeated in the design notes):
   result converted back to the 16-bit format, and the values this step
   produces decide quantised codes, so the oracle takes that decision from
   the same BF16 inputs as the kernel. The forward SwiGLU consumes the GEMM
-  result unrounded (the fused path folds the conversion into the epilogue).
+  result unrounded (the fused path folds the conversion into the epilogue);
+* in the MXFP8 mode with MXFP4 activations (mx == "act4") the wgrad operands
+  X and H are the FP8 -> FP4 -> column-wise FP4 chain of their row-wise MXFP8
+  copies (act4_cols_in_groups; the MXFP4 readings are in mxfp4_oracle.py);
+  everything else is as in MXFP8 mode.
 """
 from __future__ import annotations
 
