@@ -27,6 +27,8 @@ CASES = [
     (4096, 2048, 64, 6),     # fine-grained shape
     (100, 128, 256, 8),
     (1, 64, 4, 2),
+    (50, 128, 1, 1),          # a single expert: seven zero-padded expert columns
+    (77, 192, 3, 2),          # E not a multiple of 4, H not a multiple of 128
 ]
 
 
