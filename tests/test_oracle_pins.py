@@ -356,7 +356,7 @@ def test_token_permutation_invariance(mx):
         np.testing.assert_allclose(b2["dW2"], b["dW2"], rtol=1e-10, atol=1e-12)
 
 
-@pytest.mark.parametrize("mx", [False, True])
+@pytest.mark.parametrize("mx", [False, True, "act4"])
 def test_sampled_mode_equals_full_mode(mx):
     rng = np.random.default_rng(15)
     T, H, F, E, k = 200, 64, 96, 5, 2
