@@ -186,3 +186,31 @@ def test_act4_chain_is_coarser_than_mxfp8():
     scale = np.ldexp(1.0, np.floor(np.log2(amax)).astype(int) - 2)
     err = np.abs(O.act4_cols_in_groups(x) - x).reshape(3, 32, 64)
     assert np.all(err <= 2.0 * scale[:, None, :] + 2.0 ** -4 * amax[:, None, :])
+
+
+def test_planted_mxfp4_mistakes_are_caught(monkeypatch):
+    """Plausible slips in the MXFP4 oracle fail the pins above: the E4M3
+    exponent offset (8) in place of E2M1's (2); ties rounded away from zero;
+    row -> column reusing the row scales."""
+    # wrong emax: the all-ones block would get scale 2^-8 and saturate
+    with monkeypatch.context() as m:
+        m.setattr(Q, "E2M1_EMAX", 8)
+        c, s = Q.mx4_quantize(np.ones((1, 32)), axis=1)
+        assert not (s[0, 0] == 125 and (c == 6).all())
+    # ties away from zero: 0.25 -> 0.5 and 2.5 -> 3 instead of 0 and 2
+    def away(a):
+        a = np.minimum(np.asarray(a, dtype=float), 6.0)
+        d = np.abs(a[..., None] - Q.E2M1_VALUES)
+        # the larger of two equidistant candidates
+        return (7 - np.argmin(d[..., ::-1], axis=-1)).astype(np.uint8)
+    assert int(away(np.array(0.25))) != 0 and int(away(np.array(2.5))) != 4
+    # reusing row scales for the column blocks keeps 0.125 instead of rounding it to 0
+    x = np.zeros((32, 32))
+    x[0, 0] = 6.0
+    x[1:, 0] = 0.125
+    x[1:, 1] = 0.125
+    c4, s4 = Q.mx4_quantize(x, axis=1)
+    v = Q.mx4_dequantize(c4, s4, axis=1)  # row scales applied: 0.125 survives
+    assert v[5, 0] == 0.125
+    cc, sc = Q.mxfp4_row_to_col(c4, s4)
+    assert Q.mx4_dequantize(cc, sc, axis=1)[0, 5] == 0.0  # the real conversion drops it
