@@ -59,3 +59,30 @@ def test_mxfp4_argument_checks(libmoe):
         assert fn(16, 16, 100, 128, 16, 16, None) == 1, name   # rows % 128
         assert fn(16, 16, 128, 96, 16, 16, None) == 1, name    # cols % 128
         assert fn(8, 16, 128, 128, 16, 16, None) == 1, name    # misaligned data
+
+
+def test_layer_workspace_layouts(libmoe):
+    """Host-only layout queries: the MXFP4-activation mode adds exactly the
+    row-wise MXFP4 copies of x and H (half a byte per element plus scales) to
+    the MXFP8 layout; parts of another precision have size 0; unsupported
+    configs report size 0 (H % 256 for the MXFP8 modes, align % 128)."""
+    from mixture_experts_expert_sort_b300 import binding as B
+    T, H, F, E, k = 16384, 4096, 14336, 8, 2
+    c8 = B.layer_config(T, H, F, E, k, "mxfp8")
+    c4 = B.layer_config(T, H, F, E, k, "mxfp8_act4")
+    cb = B.layer_config(T, H, F, E, k, "bf16")
+    R = B.moe_rows_padded_max(T, E, k, 128)
+    R = -(-R // 128) * 128
+    scale = lambda mn, kd: (mn // 128) * (kd // 128) * 512  # noqa: E731
+    extra = [R * H // 2, scale(R, H), R * F // 2, scale(R, F)]
+    up = lambda b: -(-b // 256) * 256  # noqa: E731
+    assert B.moe_layer_workspace_size(c4) == B.moe_layer_workspace_size(c8) + sum(map(up, extra))
+    for name, want in zip(("x4_q_row", "x4_s_row", "h4_q_row", "h4_s_row"), extra):
+        part = B.PARTS[name][0]
+        assert B.moe_layer_workspace_part(c4, part)[1] == want, name
+        assert B.moe_layer_workspace_part(c8, part)[1] == 0, name
+    assert B.moe_layer_workspace_part(cb, B.PARTS["x_q_row"][0])[1] == 0
+    assert B.moe_layer_workspace_part(c8, B.PARTS["xp"][0])[1] == 0
+    assert B.moe_layer_workspace_size(B.layer_config(64, 384, 256, 4, 2, "mxfp8_act4")) == 0
+    assert B.moe_layer_workspace_size(B.layer_config(64, 384, 256, 4, 2, "bf16")) > 0
+    assert B.moe_layer_workspace_size(B.layer_config(64, 256, 256, 4, 2, "bf16", align=64)) == 0
