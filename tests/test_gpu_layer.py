@@ -3,7 +3,7 @@ oracle's per-expert loop, on the seeded synthetic workloads.
 
 Integer results (routing indices, counts, offsets, dest, src) must match
 bit-exactly. Float results must have relative Frobenius error <= 5e-3 and
-max-abs error <= 1e-2 * max|ref| (the BF16 tolerance of the benchmark spec).
+max-abs error <= 1e-2 * max|ref| (the BF16 tolerance the layer is held to).
 """
 import numpy as np
 import pytest

@@ -6,7 +6,7 @@ scale the layer computes from inputs that both sides hold identically (x and
 dOut gathered into expert order, W1 and W2, each row- and column-wise).
 Float results (out, dX, dW1, dW2, dlogits) must have relative Frobenius error
 <= 1e-2 against the oracle emulating the same quantisation (the MXFP8
-tolerance of the benchmark spec). Quantised intermediates (H, dY1) come from
+tolerance the layer is held to). Quantised intermediates (H, dY1) come from
 fp32 accumulators whose summation order differs from the oracle's, so they
 are covered by that tolerance rather than compared byte for byte.
 """
