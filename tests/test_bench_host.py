@@ -1,6 +1,12 @@
-"""Host-side logic of bench.py that needs no GPU: the clock record keeps the
-nvidia-smi samples taken inside the timed region and reports their median
-and throttle reasons (all samples when none fell inside)."""
+"""Host-side logic of bench.py that needs no GPU.
+
+* The clock record keeps the nvidia-smi samples taken inside the timed region
+  and reports their median and throttle reasons (all samples when none fell
+  inside).
+* The algorithmic work per launch (the numerator of every roofline fraction)
+  equals counts taken from the oracle: GEMM multiply-adds from the operand
+  shapes of its per-expert loop, quantiser bytes from the sizes of the MXFP8
+  and MXFP4 copies it produces."""
 import datetime
 import os
 import sys
@@ -55,3 +61,91 @@ def test_clock_record_falls_back_to_all_samples():
     lines = [_line(base, 1000), _line(base + 50 * ms, 2000)]
     r = _sampler(lines, base + 10 * ms, base + 20 * ms).stop()
     assert r["samples_in_timed_region"] == 0 and r["sm_mhz"] == 1500
+
+
+# ---------------------------------------------------------------------------
+# The algorithmic work behind every roofline fraction, counted independently
+# ---------------------------------------------------------------------------
+
+import numpy as np  # noqa: E402
+import pytest  # noqa: E402
+
+from mixture_experts_expert_sort_b300 import inputs as I  # noqa: E402
+from oracle import moe_oracle as O  # noqa: E402
+from oracle import mxfp4_oracle as M  # noqa: E402
+
+GEMMS = ("fc1_swiglu", "fc2", "fc2_dgrad_swiglu_bwd", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad")
+
+
+def _np(t):
+    return t.float().numpy()
+
+
+def test_gemm_flops_count_the_oracle_loop():
+    """Each GEMM's flops = 2 x the multiply-adds of the oracle's per-expert
+    matmuls, with each expert's row count taken from the routing the loop
+    actually did (one expert receives no token)."""
+    wl = I.Workload("count", 96, 128, 256, 4, 2, "mxfp8", 11, zipf_s=1.0, zero_experts=1)
+    inp = I.make_all(wl)
+    macs = dict.fromkeys(GEMMS, 0)
+    rows = []
+    for e, tok, slot, y2, dxp, dp, dW1e, dW2e in O.layer_fwd_bwd_expert_stream(
+            _np(inp["x"]), inp["logits"].numpy(), _np(inp["w1"]), _np(inp["w2"]),
+            _np(inp["dout"]), wl.k):
+        n = len(tok)
+        h, f2 = dW1e.shape  # W1_e is [H, 2F]
+        f, h_out = dW2e.shape  # W2_e is [F, H]
+        assert y2.shape == (n, h_out) and dxp.shape == (n, h)
+        rows.append(n)
+        macs["fc1_swiglu"] += n * h * f2  # X_e [n, H] @ W1_e
+        macs["fc2"] += n * f * h_out  # H_e [n, F] @ W2_e
+        macs["fc2_dgrad_swiglu_bwd"] += n * h_out * f  # dY2_e [n, H] @ W2_e^T
+        macs["fc2_wgrad"] += f * n * h_out  # H_e^T [F, n] @ dY2_e
+        macs["fc1_dgrad"] += n * f2 * h  # dY1_e [n, 2F] @ W1_e^T
+        macs["fc1_wgrad"] += h * n * f2  # X_e^T [H, n] @ dY1_e
+    assert 0 in rows and sum(rows) == wl.T * wl.k
+    work = bench.kernel_work(wl)
+    for name in GEMMS:
+        assert work[name] == ("flops", pytest.approx(2.0 * macs[name])), name
+    assert sum(work[n][1] for n in GEMMS) == pytest.approx(wl.gemm_flops_fwd_bwd())
+
+
+def _mx8_bytes(c, s):
+    return c.nbytes + s.nbytes
+
+
+def test_quantiser_bytes_are_the_oracle_outputs():
+    """Quantiser traffic = the input it must read once + the bytes of every
+    MXFP8 / MXFP4 copy the oracle produces for the same operand."""
+    wl = I.Workload("bytes", 64, 128, 256, 2, 2, "mxfp8", 12)
+    work = bench.kernel_work(wl)
+    w1, w2 = _np(I.make_w1(wl)), _np(I.make_w2(wl))
+    both = lambda a: sum(_mx8_bytes(*O.mx_quantize(a, axis=ax)) for ax in (0, 1))  # noqa: E731
+    assert work["quant_w1"] == ("bytes", pytest.approx(2 * w1.size + sum(both(w) for w in w1)))
+    assert work["quant_w2"] == ("bytes", pytest.approx(2 * w2.size + sum(both(w) for w in w2)))
+    # activations: x is read once per token (T rows), R = T*k gathered rows written
+    x = _np(I.make_x(wl))
+    xg = np.repeat(x, wl.k, axis=0)
+    assert work["quant_x"] == ("bytes", pytest.approx(2 * x.size + both(xg)))
+    assert work["quant_dout"] == ("bytes", pytest.approx(2 * x.size + both(xg)))
+
+
+def test_mxfp4_conversion_bytes_are_the_oracle_outputs():
+    """MXFP4 activation mode: the FP8 -> FP4 copies read one row-wise MXFP8
+    copy and write packed E2M1 codes + scales; the rebuilt column-wise MXFP8
+    operand reads the FP4 copy and writes codes + scales."""
+    wl = I.Workload("bytes4", 64, 128, 256, 2, 2, "mxfp8_act4", 13)
+    work = bench.kernel_work(wl)
+    R = wl.T * wl.k
+    for name, cols in (("x", wl.H), ("h", wl.F)):
+        a = np.random.default_rng(5).standard_normal((R, cols))
+        c8, s8 = O.mx_quantize(a, axis=1)
+        c4, s4 = M.mxfp4_from_mxfp8(c8, s8)
+        fp4 = M.pack_e2m1(c4).nbytes + s4.nbytes
+        col8 = _mx8_bytes(*M.mxfp8_col_from_mxfp4_row(c4, s4))
+        assert work[f"{name}_to_fp4"] == ("bytes", pytest.approx(_mx8_bytes(c8, s8) + fp4))
+        assert work[f"{name}_col_from_fp4"] == ("bytes", pytest.approx(fp4 + col8))
+    # this mode quantises x row-wise only (the column-wise copy is rebuilt later)
+    x = _np(I.make_x(wl))
+    row = _mx8_bytes(*O.mx_quantize(np.repeat(x, wl.k, axis=0), axis=1))
+    assert work["quant_x"] == ("bytes", pytest.approx(2 * x.size + row))
