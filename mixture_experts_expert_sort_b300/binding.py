@@ -1,8 +1,10 @@
 """Thin ctypes binding of libmoe (include/moe.h): argument marshalling only.
 
-Every function here takes torch CUDA tensors, checks nothing beyond what
-ctypes needs, passes raw device pointers and the current CUDA stream to the C
-entry point of the same name, and raises on a non-zero status. All
+Every function here takes torch CUDA tensors, checks that each one is dense
+device memory (the C entry points take plain pointers, so a host tensor would
+reach a kernel as an invalid address and a strided view would be read as if
+it were dense), passes raw device pointers and the current CUDA stream to the
+C entry point of the same name, and raises on a non-zero status. All
 computation happens in the library's kernels; if the library is missing this
 module raises instead of computing anything elsewhere.
 """
@@ -90,7 +92,29 @@ def _check(status: int, what: str):
 
 
 def ptr(t):
-    return None if t is None else t.data_ptr()
+    """Device address of a dense (contiguous) CUDA tensor; None stays None."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise MoeError(f"tensor of shape {tuple(t.shape)} with strides {t.stride()} is not "
+                       "contiguous: the library reads every operand as a dense array")
+    return _device_address(t)
+
+
+def ptr_rows(t):
+    """Device address of a CUDA matrix whose rows may be strided (the caller
+    passes t.stride(0) as the leading dimension) but are dense within."""
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1) or t.stride(0) < t.shape[1]:
+        raise MoeError(f"tensor of shape {tuple(t.shape)} with strides {t.stride()} is not a "
+                       "matrix of dense rows")
+    return _device_address(t)
+
+
+def _device_address(t):
+    if t.device.type != "cuda":
+        raise MoeError(f"a {t.device.type} tensor was passed where the library needs device "
+                       "memory")
+    return t.data_ptr()
 
 
 def stream_handle(stream=None):
@@ -130,9 +154,9 @@ def moe_route_backward(dp, w, idx, E, dest=None, dlogits=None, stream=None):
     dp2 = dp if dp.dim() == 2 else dp.reshape(-1, 1)
     dlogits = dlogits if dlogits is not None else torch.empty((T, E), dtype=torch.float32,
                                                               device=idx.device)
-    _check(lib().moe_route_backward(ptr(dp2), dp2.stride(0), dp2.shape[1], ptr(dest), ptr(w),
-                                    ptr(idx), T, E, k, ptr(dlogits), stream_handle(stream)),
-           "moe_route_backward")
+    _check(lib().moe_route_backward(ptr_rows(dp2), dp2.stride(0), dp2.shape[1], ptr(dest),
+                                    ptr(w), ptr(idx), T, E, k, ptr(dlogits),
+                                    stream_handle(stream)), "moe_route_backward")
     return dlogits
 
 
@@ -281,7 +305,7 @@ def mxfp8_quantize(x, dirs=QUANT_ROWWISE | QUANT_COLWISE, rows=None, src=None, s
         if dirs & QUANT_COLWISE:
             out["q_col"] = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
             out["s_col"] = torch.empty(mx_scale_bytes(cols, rows), dtype=torch.uint8, device=dev)
-    _check(lib().mxfp8_quantize(ptr(x), rows, cols, x.stride(0), ptr(src), src_div, dirs,
+    _check(lib().mxfp8_quantize(ptr_rows(x), rows, cols, x.stride(0), ptr(src), src_div, dirs,
                                 ptr(out.get("q_row")), ptr(out.get("s_row")),
                                 ptr(out.get("q_col")), ptr(out.get("s_col")),
                                 stream_handle(stream)), "mxfp8_quantize")

@@ -19,9 +19,25 @@ class MoELayer:
         self.device = torch.device(device)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
 
+    def _expect(self, **named):
+        """Each operand must have the shape and dtype the library's layer
+        entry points take (the C ABI sees only pointers)."""
+        T, H, F, E = self.T, self.H, self.F, self.E
+        want = {"logits": ((T, E), torch.float32), "dlogits": ((T, E), torch.float32),
+                "x": ((T, H), torch.bfloat16), "out": ((T, H), torch.bfloat16),
+                "dout": ((T, H), torch.bfloat16), "dx": ((T, H), torch.bfloat16),
+                "w1": ((E, H, 2 * F), torch.bfloat16), "dw1": ((E, H, 2 * F), torch.bfloat16),
+                "w2": ((E, F, H), torch.bfloat16), "dw2": ((E, F, H), torch.bfloat16)}
+        for name, t in named.items():
+            shape, dtype = want[name]
+            if tuple(t.shape) != shape or t.dtype != dtype:
+                raise B.MoeError(f"{name}: expected {dtype} {list(shape)}, got {t.dtype} "
+                                 f"{list(t.shape)}")
+
     def forward(self, logits, x, w1, w2, out=None, stream=None):
         out = out if out is not None else torch.empty((self.T, self.H), dtype=torch.bfloat16,
                                                       device=self.device)
+        self._expect(logits=logits, x=x, w1=w1, w2=w2, out=out)
         return B.moe_layer_forward(self.cfg, logits, x, w1, w2, out, self.workspace, stream)
 
     def backward(self, dout, w1, w2, dx=None, dw1=None, dw2=None, dlogits=None, stream=None):
@@ -34,6 +50,7 @@ class MoELayer:
                                                       dtype=torch.bfloat16, device=dev)
         dlogits = dlogits if dlogits is not None else torch.empty((self.T, self.E),
                                                                   dtype=torch.float32, device=dev)
+        self._expect(dout=dout, w1=w1, w2=w2, dx=dx, dw1=dw1, dw2=dw2, dlogits=dlogits)
         return B.moe_layer_backward(self.cfg, dout, w1, w2, dx, dw1, dw2, dlogits, self.workspace,
                                     stream)
 

@@ -86,3 +86,50 @@ def test_layer_workspace_layouts(libmoe):
     assert B.moe_layer_workspace_size(B.layer_config(64, 384, 256, 4, 2, "mxfp8_act4")) == 0
     assert B.moe_layer_workspace_size(B.layer_config(64, 384, 256, 4, 2, "bf16")) > 0
     assert B.moe_layer_workspace_size(B.layer_config(64, 256, 256, 4, 2, "bf16", align=64)) == 0
+
+
+def test_binding_refuses_host_and_strided_tensors():
+    """The library takes plain device pointers: the binding refuses a host
+    tensor (it would reach a kernel as an invalid address) and a strided view
+    (it would be read as if dense) before any call is made."""
+    import torch
+    from mixture_experts_expert_sort_b300 import binding as B
+    with pytest.raises(B.MoeError, match="cpu tensor"):
+        B.ptr(torch.zeros(4, 8))
+    with pytest.raises(B.MoeError, match="not contiguous"):
+        B.ptr(torch.zeros(8, 4).t())
+    with pytest.raises(B.MoeError, match="not contiguous"):
+        B.ptr(torch.zeros(4, 8)[:, :4])
+    assert B.ptr(None) is None
+    # leading-dimension operands: strided rows pass the layout check (and then
+    # fail only for being host memory); strided columns do not
+    with pytest.raises(B.MoeError, match="cpu tensor"):
+        B.ptr_rows(torch.zeros(4, 16)[:, :8])
+    with pytest.raises(B.MoeError, match="dense rows"):
+        B.ptr_rows(torch.zeros(8, 4).t())
+    with pytest.raises(B.MoeError, match="dense rows"):
+        B.ptr_rows(torch.zeros(4, 8, 2))
+
+
+def test_layer_checks_operand_shapes_and_dtypes(libmoe):
+    """MoELayer checks every operand against the shapes and dtypes of the
+    layer entry points before the library sees a pointer."""
+    import torch
+    from mixture_experts_expert_sort_b300 import binding as B
+    from mixture_experts_expert_sort_b300.layer import MoELayer
+    T, H, F, E, k = 64, 128, 256, 4, 2
+    L = MoELayer(T, H, F, E, k, device="cpu")
+    bf = torch.bfloat16
+    lg, x = torch.zeros(T, E), torch.zeros(T, H, dtype=bf)
+    w1, w2 = torch.zeros(E, H, 2 * F, dtype=bf), torch.zeros(E, F, H, dtype=bf)
+    with pytest.raises(B.MoeError, match="logits: expected"):
+        L.forward(lg.to(bf), x, w1, w2)
+    with pytest.raises(B.MoeError, match="w1: expected"):
+        L.forward(lg, x, w1.transpose(1, 2).contiguous(), w2)
+    with pytest.raises(B.MoeError, match="x: expected"):
+        L.forward(lg, x[: T - 1], w1, w2)
+    with pytest.raises(B.MoeError, match="dw2: expected"):
+        L.backward(x, w1, w2, dw2=torch.zeros(E, F, H))
+    # right shapes and dtypes, but host memory: refused at the pointer
+    with pytest.raises(B.MoeError, match="cpu tensor"):
+        L.forward(lg, x, w1, w2)
