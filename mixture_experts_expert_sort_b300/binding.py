@@ -1,10 +1,11 @@
 """Thin ctypes binding of libmoe (include/moe.h): argument marshalling only.
 
 Every function here takes torch CUDA tensors, checks that each one is dense
-device memory (the C entry points take plain pointers, so a host tensor would
-reach a kernel as an invalid address and a strided view would be read as if
-it were dense), passes raw device pointers and the current CUDA stream to the
-C entry point of the same name, and raises on a non-zero status. All
+device memory of the element type the C declaration documents (the entry
+points take plain pointers, so a host tensor would reach a kernel as an
+invalid address, a strided view would be read as if it were dense and a wrong
+dtype would be reinterpreted), passes raw device pointers and the current CUDA
+stream to the C entry point of the same name, and raises on a non-zero status. All
 computation happens in the library's kernels; if the library is missing this
 module raises instead of computing anything elsewhere.
 """
@@ -91,27 +92,38 @@ def _check(status: int, what: str):
         raise MoeError(f"{what} failed: {msg}")
 
 
-def ptr(t):
-    """Device address of a dense (contiguous) CUDA tensor; None stays None."""
+BF16, F32, I32, U8 = torch.bfloat16, torch.float32, torch.int32, torch.uint8
+
+
+def ptr(t, dtype=None):
+    """Device address of a dense (contiguous) CUDA tensor of element type
+    `dtype` (the type the C declaration documents); None stays None."""
     if t is None:
         return None
     if not t.is_contiguous():
         raise MoeError(f"tensor of shape {tuple(t.shape)} with strides {t.stride()} is not "
                        "contiguous: the library reads every operand as a dense array")
-    return _device_address(t)
+    return _device_address(t, dtype)
 
 
-def ptr_rows(t):
+def ptr_rows(t, dtype=None):
     """Device address of a CUDA matrix whose rows may be strided (the caller
     passes t.stride(0) as the leading dimension) but are dense within."""
     if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1) or t.stride(0) < t.shape[1]:
         raise MoeError(f"tensor of shape {tuple(t.shape)} with strides {t.stride()} is not a "
                        "matrix of dense rows")
-    return _device_address(t)
+    return _device_address(t, dtype)
 
 
-def _device_address(t):
-    if t.device.type != "cuda":
+def _is_device(t):
+    return t.device.type == "cuda"
+
+
+def _device_address(t, dtype):
+    if dtype is not None and t.dtype != dtype:
+        raise MoeError(f"tensor of shape {tuple(t.shape)} has element type {t.dtype}; the "
+                       f"library reads this argument as {dtype}")
+    if not _is_device(t):
         raise MoeError(f"a {t.device.type} tensor was passed where the library needs device "
                        "memory")
     return t.data_ptr()
@@ -143,8 +155,8 @@ def moe_route(logits, k, idx=None, w=None, stream=None):
     dev = logits.device
     idx = idx if idx is not None else torch.empty((T, k), dtype=torch.int32, device=dev)
     w = w if w is not None else torch.empty((T, k), dtype=torch.float32, device=dev)
-    _check(lib().moe_route(ptr(logits), T, E, k, ptr(idx), ptr(w), stream_handle(stream)),
-           "moe_route")
+    _check(lib().moe_route(ptr(logits, F32), T, E, k, ptr(idx, I32), ptr(w, F32),
+                           stream_handle(stream)), "moe_route")
     return idx, w
 
 
@@ -154,8 +166,8 @@ def moe_route_backward(dp, w, idx, E, dest=None, dlogits=None, stream=None):
     dp2 = dp if dp.dim() == 2 else dp.reshape(-1, 1)
     dlogits = dlogits if dlogits is not None else torch.empty((T, E), dtype=torch.float32,
                                                               device=idx.device)
-    _check(lib().moe_route_backward(ptr_rows(dp2), dp2.stride(0), dp2.shape[1], ptr(dest),
-                                    ptr(w), ptr(idx), T, E, k, ptr(dlogits),
+    _check(lib().moe_route_backward(ptr_rows(dp2, F32), dp2.stride(0), dp2.shape[1], ptr(dest, I32),
+                                    ptr(w, F32), ptr(idx, I32), T, E, k, ptr(dlogits, F32),
                                     stream_handle(stream)), "moe_route_backward")
     return dlogits
 
@@ -179,10 +191,10 @@ def moe_router_forward(x, w_r, k, workspace=None, stream=None, out=None):
                "aux": torch.empty(1 + 2 * E, dtype=torch.float32, device=dev)}
     if workspace is None:
         workspace = torch.empty(moe_router_workspace_size(T, H, E), dtype=torch.uint8, device=dev)
-    _check(lib().moe_router_forward(ptr(x), ptr(w_r), T, H, E, k, ptr(out["logits"]),
-                                    ptr(out["idx"]), ptr(out["w"]), ptr(out["aux"]),
-                                    ptr(workspace), workspace.numel(), stream_handle(stream)),
-           "moe_router_forward")
+    _check(lib().moe_router_forward(ptr(x, BF16), ptr(w_r, BF16), T, H, E, k,
+                                    ptr(out["logits"], F32), ptr(out["idx"], I32),
+                                    ptr(out["w"], F32), ptr(out["aux"], F32), ptr(workspace, U8),
+                                    workspace.numel(), stream_handle(stream)), "moe_router_forward")
     return out
 
 
@@ -198,9 +210,10 @@ def moe_router_backward(x, w_r, logits, aux, dlogits_route, aux_coeff, dx_in=Non
     dw_r = dw_r if dw_r is not None else torch.empty((H, E), dtype=torch.bfloat16, device=dev)
     if workspace is None:
         workspace = torch.empty(moe_router_workspace_size(T, H, E), dtype=torch.uint8, device=dev)
-    _check(lib().moe_router_backward(ptr(x), ptr(w_r), ptr(logits), ptr(aux), ptr(dlogits_route),
-                                     float(aux_coeff), T, H, E, ptr(dlogits), ptr(dx_in),
-                                     ptr(dx_out), ptr(dw_r), ptr(workspace), workspace.numel(),
+    _check(lib().moe_router_backward(ptr(x, BF16), ptr(w_r, BF16), ptr(logits, F32), ptr(aux, F32),
+                                     ptr(dlogits_route, F32), float(aux_coeff), T, H, E,
+                                     ptr(dlogits, F32), ptr(dx_in, BF16), ptr(dx_out, BF16),
+                                     ptr(dw_r, BF16), ptr(workspace, U8), workspace.numel(),
                                      stream_handle(stream)), "moe_router_backward")
     return dlogits, dx_out, dw_r
 
@@ -230,10 +243,10 @@ def moe_permute_plan(idx, E, align, src_rows=None, workspace=None, stream=None, 
     wsb = moe_permute_plan_workspace_size(T, E, k)
     if workspace is None:
         workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    _check(lib().moe_permute_plan(ptr(idx), T, E, k, align, ptr(out["counts"]),
-                                  ptr(out["offsets"]), ptr(out["dest"]), ptr(out["src"]),
-                                  src_rows, ptr(workspace), workspace.numel(),
-                                  stream_handle(stream)), "moe_permute_plan")
+    _check(lib().moe_permute_plan(ptr(idx, I32), T, E, k, align, ptr(out["counts"], I32),
+                                  ptr(out["offsets"], I32), ptr(out["dest"], I32),
+                                  ptr(out["src"], I32), src_rows, ptr(workspace, U8),
+                                  workspace.numel(), stream_handle(stream)), "moe_permute_plan")
     return out
 
 
@@ -254,9 +267,9 @@ def moe_permute_plan_static(idx, E, align, src_rows=None, stream=None, out=None)
             "dest": torch.empty(max(T * k, 1), dtype=torch.int32, device=dev),
             "src": torch.empty(max(src_rows, 1), dtype=torch.int32, device=dev),
         }
-    st = lib().moe_permute_plan_static(ptr(idx), T, E, k, align, ptr(out["counts"]),
-                                       ptr(out["offsets"]), ptr(out["dest"]), ptr(out["src"]),
-                                       src_rows, stream_handle(stream))
+    st = lib().moe_permute_plan_static(ptr(idx, I32), T, E, k, align, ptr(out["counts"], I32),
+                                       ptr(out["offsets"], I32), ptr(out["dest"], I32),
+                                       ptr(out["src"], I32), src_rows, stream_handle(stream))
     if st == MOE_ERR_UNSUPPORTED:
         raise MoeError(f"moe_permute_plan_static: ceil(T*k/1024)*E = "
                        f"{-(-T * k // 1024) * E} exceeds the static scratch of "
@@ -272,15 +285,16 @@ def moe_permute(x, dest, offsets, counts, k, rows, w=None, xp=None, p_rows=None,
     xp = xp if xp is not None else torch.empty((rows, H), dtype=x.dtype, device=dev)
     if w is not None and p_rows is None:
         p_rows = torch.empty(rows, dtype=torch.float32, device=dev)
-    _check(lib().moe_permute(ptr(x), ptr(dest), ptr(offsets), ptr(counts), ptr(w), T, H, E, k,
-                             ptr(xp), ptr(p_rows), stream_handle(stream)), "moe_permute")
+    _check(lib().moe_permute(ptr(x, BF16), ptr(dest, I32), ptr(offsets, I32), ptr(counts, I32),
+                             ptr(w, F32), T, H, E, k, ptr(xp, BF16), ptr(p_rows, F32),
+                             stream_handle(stream)), "moe_permute")
     return xp, p_rows
 
 
 def moe_unpermute(y, dest, T, k, w=None, out=None, stream=None):
     H = y.shape[1]
     out = out if out is not None else torch.empty((T, H), dtype=y.dtype, device=y.device)
-    _check(lib().moe_unpermute(ptr(y), ptr(dest), ptr(w), T, H, k, ptr(out),
+    _check(lib().moe_unpermute(ptr(y, BF16), ptr(dest, I32), ptr(w, F32), T, H, k, ptr(out, BF16),
                                stream_handle(stream)), "moe_unpermute")
     return out
 
@@ -305,9 +319,9 @@ def mxfp8_quantize(x, dirs=QUANT_ROWWISE | QUANT_COLWISE, rows=None, src=None, s
         if dirs & QUANT_COLWISE:
             out["q_col"] = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
             out["s_col"] = torch.empty(mx_scale_bytes(cols, rows), dtype=torch.uint8, device=dev)
-    _check(lib().mxfp8_quantize(ptr_rows(x), rows, cols, x.stride(0), ptr(src), src_div, dirs,
-                                ptr(out.get("q_row")), ptr(out.get("s_row")),
-                                ptr(out.get("q_col")), ptr(out.get("s_col")),
+    _check(lib().mxfp8_quantize(ptr_rows(x, BF16), rows, cols, x.stride(0), ptr(src, I32), src_div,
+                                dirs, ptr(out.get("q_row"), U8), ptr(out.get("s_row"), U8),
+                                ptr(out.get("q_col"), U8), ptr(out.get("s_col"), U8),
                                 stream_handle(stream)), "mxfp8_quantize")
     return out
 
@@ -324,8 +338,8 @@ def mxfp4_from_mxfp8(q8, s8, stream=None, out=None):
     rows, cols = q8.shape
     out = out or {"q4": _u8((rows, cols // 2), q8.device),
                   "s4": _u8(mx_scale_bytes(rows, cols), q8.device)}
-    _check(lib().mxfp4_from_mxfp8(ptr(q8), ptr(s8), rows, cols, ptr(out["q4"]), ptr(out["s4"]),
-                                  stream_handle(stream)), "mxfp4_from_mxfp8")
+    _check(lib().mxfp4_from_mxfp8(ptr(q8, U8), ptr(s8, U8), rows, cols, ptr(out["q4"], U8),
+                                  ptr(out["s4"], U8), stream_handle(stream)), "mxfp4_from_mxfp8")
     return out
 
 
@@ -335,8 +349,8 @@ def mxfp8_from_mxfp4(q4, s4, stream=None, out=None):
     cols = 2 * half
     out = out or {"q8": _u8((rows, cols), q4.device),
                   "s8": _u8(mx_scale_bytes(rows, cols), q4.device)}
-    _check(lib().mxfp8_from_mxfp4(ptr(q4), ptr(s4), rows, cols, ptr(out["q8"]), ptr(out["s8"]),
-                                  stream_handle(stream)), "mxfp8_from_mxfp4")
+    _check(lib().mxfp8_from_mxfp4(ptr(q4, U8), ptr(s4, U8), rows, cols, ptr(out["q8"], U8),
+                                  ptr(out["s8"], U8), stream_handle(stream)), "mxfp8_from_mxfp4")
     return out
 
 
@@ -347,8 +361,8 @@ def mxfp4_rowwise_to_colwise(q4, s4, stream=None, out=None):
     cols = 2 * half
     out = out or {"q4c": _u8((cols, rows // 2), q4.device),
                   "s4c": _u8(mx_scale_bytes(cols, rows), q4.device)}
-    _check(lib().mxfp4_rowwise_to_colwise(ptr(q4), ptr(s4), rows, cols, ptr(out["q4c"]),
-                                          ptr(out["s4c"]), stream_handle(stream)),
+    _check(lib().mxfp4_rowwise_to_colwise(ptr(q4, U8), ptr(s4, U8), rows, cols, ptr(out["q4c"], U8),
+                                          ptr(out["s4c"], U8), stream_handle(stream)),
            "mxfp4_rowwise_to_colwise")
     return out
 
@@ -360,8 +374,9 @@ def mxfp8_colwise_from_mxfp4_rowwise(q4, s4, stream=None, out=None):
     cols = 2 * half
     out = out or {"q8c": _u8((cols, rows), q4.device),
                   "s8c": _u8(mx_scale_bytes(cols, rows), q4.device)}
-    _check(lib().mxfp8_colwise_from_mxfp4_rowwise(ptr(q4), ptr(s4), rows, cols, ptr(out["q8c"]),
-                                                  ptr(out["s8c"]), stream_handle(stream)),
+    _check(lib().mxfp8_colwise_from_mxfp4_rowwise(ptr(q4, U8), ptr(s4, U8), rows, cols,
+                                                  ptr(out["q8c"], U8), ptr(out["s8c"], U8),
+                                                  stream_handle(stream)),
            "mxfp8_colwise_from_mxfp4_rowwise")
     return out
 
@@ -380,9 +395,9 @@ def moe_grouped_gemm_bf16(mode, A, B, offsets, b_layout=0, M=0, N=0, K=0, C=None
     else:
         M, N = A.shape[1], B.shape[1]
         C = C if C is not None else torch.empty((E, M, N), dtype=torch.bfloat16, device=A.device)
-    _check(lib().moe_grouped_gemm_bf16(mode, ptr(A), ptr(B), b_layout, ptr(offsets), E, rows, M,
-                                       N, K, ptr(C), stream_handle(stream)),
-           "moe_grouped_gemm_bf16")
+    _check(lib().moe_grouped_gemm_bf16(mode, ptr(A, BF16), ptr(B, BF16), b_layout,
+                                       ptr(offsets, I32), E, rows, M, N, K, ptr(C, BF16),
+                                       stream_handle(stream)), "moe_grouped_gemm_bf16")
     return C
 
 
@@ -392,9 +407,9 @@ def moe_fc1_swiglu_bf16(xp, w1, offsets, p_rows, gu=None, h=None, stream=None):
     F = F2 // 2
     gu = gu if gu is not None else torch.empty((rows, F2), dtype=torch.bfloat16, device=xp.device)
     h = h if h is not None else torch.empty((rows, F), dtype=torch.bfloat16, device=xp.device)
-    _check(lib().moe_fc1_swiglu_bf16(ptr(xp), ptr(w1), ptr(offsets), ptr(p_rows), E, rows, H, F,
-                                     ptr(gu), ptr(h), stream_handle(stream)),
-           "moe_fc1_swiglu_bf16")
+    _check(lib().moe_fc1_swiglu_bf16(ptr(xp, BF16), ptr(w1, BF16), ptr(offsets, I32),
+                                     ptr(p_rows, F32), E, rows, H, F, ptr(gu, BF16), ptr(h, BF16),
+                                     stream_handle(stream)), "moe_fc1_swiglu_bf16")
     return gu, h
 
 
@@ -410,8 +425,9 @@ def moe_fc2_dgrad_swiglu_bwd_bf16(dy2, w2, offsets, p_rows, gu, dy1=None, dp_par
     dy1 = dy1 if dy1 is not None else torch.empty((rows, 2 * F), dtype=torch.bfloat16, device=dev)
     if dp_part is None:
         dp_part = torch.empty((rows, moe_swiglu_bwd_parts(F)), dtype=torch.float32, device=dev)
-    _check(lib().moe_fc2_dgrad_swiglu_bwd_bf16(ptr(dy2), ptr(w2), ptr(offsets), ptr(p_rows),
-                                               ptr(gu), E, rows, H, F, ptr(dy1), ptr(dp_part),
+    _check(lib().moe_fc2_dgrad_swiglu_bwd_bf16(ptr(dy2, BF16), ptr(w2, BF16), ptr(offsets, I32),
+                                               ptr(p_rows, F32), ptr(gu, BF16), E, rows, H, F,
+                                               ptr(dy1, BF16), ptr(dp_part, F32),
                                                stream_handle(stream)),
            "moe_fc2_dgrad_swiglu_bwd_bf16")
     return dy1, dp_part
@@ -428,10 +444,10 @@ def moe_grouped_gemm_mxfp8(mode, a, sa, b, sb, offsets, b_row_stride=0, b_k_stri
     if C is None:
         shape = (a_rows, N) if mode == GEMM_FPROP else (E, M, N)
         C = torch.empty(shape, dtype=torch.bfloat16, device=a.device)
-    _check(lib().moe_grouped_gemm_mxfp8(mode, ptr(a), ptr(sa), a_rows, a_cols, ptr(b), ptr(sb),
-                                        b_rows, b_cols, b_row_stride, b_k_stride, ptr(offsets), E,
-                                        M, N, K, ptr(C), stream_handle(stream)),
-           "moe_grouped_gemm_mxfp8")
+    _check(lib().moe_grouped_gemm_mxfp8(mode, ptr(a, U8), ptr(sa, U8), a_rows, a_cols, ptr(b, U8),
+                                        ptr(sb, U8), b_rows, b_cols, b_row_stride, b_k_stride,
+                                        ptr(offsets, I32), E, M, N, K, ptr(C, BF16),
+                                        stream_handle(stream)), "moe_grouped_gemm_mxfp8")
     return C
 
 
@@ -445,10 +461,12 @@ def moe_fc1_swiglu_mxfp8(xq, sx, w1t, sw1t, offsets, p_rows, F, stream=None, out
                "s_row": torch.empty(mx_scale_bytes(rows, F), dtype=torch.uint8, device=dev),
                "q_col": torch.empty((F, rows), dtype=torch.uint8, device=dev),
                "s_col": torch.empty(mx_scale_bytes(F, rows), dtype=torch.uint8, device=dev)}
-    _check(lib().moe_fc1_swiglu_mxfp8(ptr(xq), ptr(sx), rows, H, ptr(w1t), ptr(sw1t), ptr(offsets),
-                                      ptr(p_rows), E, F, ptr(out["gu"]), ptr(out["q_row"]),
-                                      ptr(out["s_row"]), ptr(out["q_col"]), ptr(out["s_col"]),
-                                      stream_handle(stream)), "moe_fc1_swiglu_mxfp8")
+    _check(lib().moe_fc1_swiglu_mxfp8(ptr(xq, U8), ptr(sx, U8), rows, H, ptr(w1t, U8),
+                                      ptr(sw1t, U8), ptr(offsets, I32), ptr(p_rows, F32), E, F,
+                                      ptr(out["gu"], BF16), ptr(out["q_row"], U8),
+                                      ptr(out["s_row"], U8), ptr(out["q_col"], U8),
+                                      ptr(out["s_col"], U8), stream_handle(stream)),
+           "moe_fc1_swiglu_mxfp8")
     return out
 
 
@@ -463,11 +481,12 @@ def moe_fc2_dgrad_swiglu_bwd_mxfp8(dy2q, sdy2, w2q, sw2, offsets, p_rows, gu, F,
                "q_col": torch.empty((2 * F, rows), dtype=torch.uint8, device=dev),
                "s_col": torch.empty(mx_scale_bytes(2 * F, rows), dtype=torch.uint8, device=dev),
                "dp": torch.empty((rows, 2 * -(-F // 256)), dtype=torch.float32, device=dev)}
-    _check(lib().moe_fc2_dgrad_swiglu_bwd_mxfp8(ptr(dy2q), ptr(sdy2), rows, H, ptr(w2q), ptr(sw2),
-                                                ptr(offsets), ptr(p_rows), ptr(gu), E, F,
-                                                ptr(out["q_row"]), ptr(out["s_row"]),
-                                                ptr(out["q_col"]), ptr(out["s_col"]),
-                                                ptr(out["dp"]), stream_handle(stream)),
+    _check(lib().moe_fc2_dgrad_swiglu_bwd_mxfp8(ptr(dy2q, U8), ptr(sdy2, U8), rows, H, ptr(w2q, U8),
+                                                ptr(sw2, U8), ptr(offsets, I32), ptr(p_rows, F32),
+                                                ptr(gu, BF16), E, F, ptr(out["q_row"], U8),
+                                                ptr(out["s_row"], U8), ptr(out["q_col"], U8),
+                                                ptr(out["s_col"], U8), ptr(out["dp"], F32),
+                                                stream_handle(stream)),
            "moe_fc2_dgrad_swiglu_bwd_mxfp8")
     return out
 
@@ -510,14 +529,15 @@ def moe_layer_workspace_part(cfg, part):
 
 
 def moe_layer_forward(cfg, logits, x, w1, w2, out, workspace, stream=None):
-    _check(lib().moe_layer_forward(C.byref(cfg), ptr(logits), ptr(x), ptr(w1), ptr(w2), ptr(out),
-                                   ptr(workspace), workspace.numel(), stream_handle(stream)),
-           "moe_layer_forward")
+    _check(lib().moe_layer_forward(C.byref(cfg), ptr(logits, F32), ptr(x, BF16), ptr(w1, BF16),
+                                   ptr(w2, BF16), ptr(out, BF16), ptr(workspace, U8),
+                                   workspace.numel(), stream_handle(stream)), "moe_layer_forward")
     return out
 
 
 def moe_layer_backward(cfg, dout, w1, w2, dx, dw1, dw2, dlogits, workspace, stream=None):
-    _check(lib().moe_layer_backward(C.byref(cfg), ptr(dout), ptr(w1), ptr(w2), ptr(dx), ptr(dw1),
-                                    ptr(dw2), ptr(dlogits), ptr(workspace), workspace.numel(),
+    _check(lib().moe_layer_backward(C.byref(cfg), ptr(dout, BF16), ptr(w1, BF16), ptr(w2, BF16),
+                                    ptr(dx, BF16), ptr(dw1, BF16), ptr(dw2, BF16),
+                                    ptr(dlogits, F32), ptr(workspace, U8), workspace.numel(),
                                     stream_handle(stream)), "moe_layer_backward")
     return dx, dw1, dw2, dlogits

@@ -133,3 +133,90 @@ def test_layer_checks_operand_shapes_and_dtypes(libmoe):
     # right shapes and dtypes, but host memory: refused at the pointer
     with pytest.raises(B.MoeError, match="cpu tensor"):
         L.forward(lg, x, w1, w2)
+
+
+@pytest.fixture
+def host_binding(monkeypatch):
+    """The binding with a stand-in library that accepts every call, and host
+    tensors admitted as device memory: what remains are the binding's own
+    checks of element types and layouts."""
+    from mixture_experts_expert_sort_b300 import binding as B
+
+    class _AcceptAll:
+        def __getattr__(self, name):
+            return lambda *args: 0
+
+    monkeypatch.setattr(B, "lib", lambda: _AcceptAll())
+    monkeypatch.setattr(B, "_is_device", lambda t: True)
+    monkeypatch.setattr(B, "stream_handle", lambda stream=None: None)
+    return B
+
+
+def test_binding_element_types_follow_the_header(host_binding):
+    """Every wrapper accepts operands of the element types include/moe.h
+    documents for it, and refuses a wrong one."""
+    import torch
+    B = host_binding
+    T, H, F, E, k, rows = 64, 128, 256, 4, 2, 640
+    R = T * k
+
+    def bf(*s):
+        return torch.zeros(s, dtype=torch.bfloat16)
+
+    def f32(*s):
+        return torch.zeros(s, dtype=torch.float32)
+
+    def i32(*s):
+        return torch.zeros(s, dtype=torch.int32)
+
+    def u8(*s):
+        return torch.zeros(s, dtype=torch.uint8)
+
+    off = i32(E + 1)
+    B.moe_route(f32(T, E), k)
+    B.moe_route_backward(f32(rows, 3), f32(T, k), i32(T, k), E, dest=i32(R))
+    B.moe_router_forward(bf(T, H), bf(H, E), k)
+    B.moe_router_backward(bf(T, H), bf(H, E), f32(T, E), f32(1 + 2 * E), f32(T, E), 0.01,
+                          dx_in=bf(T, H))
+    B.moe_permute_plan(i32(T, k), E, 128)
+    B.moe_permute_plan_static(i32(T, k), E, 128)
+    B.moe_permute(bf(T, H), i32(R), off, i32(E), k, rows, w=f32(T, k))
+    B.moe_unpermute(bf(rows, H), i32(R), T, k, w=f32(T, k))
+    B.mxfp8_quantize(bf(T, H), rows=rows, src=i32(rows), src_div=k)
+    B.mxfp8_quantize(bf(T, 2 * H)[:, :H])  # strided rows: the leading dimension is passed
+    B.mxfp4_from_mxfp8(u8(rows, H), u8(rows * H // 32))
+    B.mxfp8_from_mxfp4(u8(rows, H // 2), u8(rows * H // 32))
+    B.mxfp4_rowwise_to_colwise(u8(rows, H // 2), u8(rows * H // 32))
+    B.mxfp8_colwise_from_mxfp4_rowwise(u8(rows, H // 2), u8(rows * H // 32))
+    B.moe_grouped_gemm_bf16(B.GEMM_FPROP, bf(rows, H), bf(E, H, F), off)
+    B.moe_grouped_gemm_bf16(B.GEMM_WGRAD, bf(rows, H), bf(rows, F), off)
+    B.moe_fc1_swiglu_bf16(bf(rows, H), bf(E, H, 2 * F), off, f32(rows))
+    B.moe_fc2_dgrad_swiglu_bwd_bf16(bf(rows, H), bf(E, F, H), off, f32(rows), bf(rows, 2 * F))
+    B.moe_grouped_gemm_mxfp8(B.GEMM_FPROP, u8(rows, H), u8(rows * H // 32), u8(F, E * H),
+                             u8(F * E * H // 32), off, N=F)
+    B.moe_fc1_swiglu_mxfp8(u8(rows, H), u8(rows * H // 32), u8(2 * F, E * H),
+                           u8(2 * F * E * H // 32), off, f32(rows), F)
+    B.moe_fc2_dgrad_swiglu_bwd_mxfp8(u8(rows, H), u8(rows * H // 32), u8(E * F, H),
+                                     u8(E * F * H // 32), off, f32(rows), bf(rows, 2 * F), F)
+    cfg = B.layer_config(T, H, F, E, k)
+    B.moe_layer_forward(cfg, f32(T, E), bf(T, H), bf(E, H, 2 * F), bf(E, F, H), bf(T, H), u8(64))
+    B.moe_layer_backward(cfg, bf(T, H), bf(E, H, 2 * F), bf(E, F, H), bf(T, H),
+                         bf(E, H, 2 * F), bf(E, F, H), f32(T, E), u8(64))
+
+    wrong = [
+        lambda: B.moe_route(bf(T, E), k),  # logits are fp32
+        lambda: B.moe_route(f32(T, E), k, idx=torch.zeros(T, k, dtype=torch.int64)),
+        lambda: B.moe_permute_plan(torch.zeros(T, k, dtype=torch.int64), E, 128),
+        lambda: B.moe_permute(f32(T, H), i32(R), off, i32(E), k, rows),  # x is bf16
+        lambda: B.mxfp8_quantize(f32(T, H)),
+        lambda: B.mxfp4_from_mxfp8(i32(rows, H // 4), u8(rows * H // 32)),
+        lambda: B.moe_grouped_gemm_bf16(B.GEMM_FPROP, bf(rows, H), bf(E, H, F), off.long()),
+        lambda: B.moe_fc1_swiglu_bf16(bf(rows, H), bf(E, H, 2 * F), off, bf(rows)),
+        lambda: B.moe_layer_forward(cfg, bf(T, E), bf(T, H), bf(E, H, 2 * F), bf(E, F, H),
+                                    bf(T, H), u8(64)),
+        lambda: B.moe_layer_forward(cfg, f32(T, E), bf(T, H), bf(E, H, 2 * F), bf(E, F, H),
+                                    bf(T, H), f32(16)),  # the workspace is counted in bytes
+    ]
+    for call in wrong:
+        with pytest.raises(B.MoeError, match="element type"):
+            call()
