@@ -663,7 +663,7 @@ inline int logits_ntg(int E) {
 }
 inline int dw_ntg(int E) {
   const int nt = (E + 7) / 8;
-  return nt >= 3 ? 4 : nt;
+  return nt >= 2 ? 2 : 1;  // four n-tiles' accumulators would not fit two CTAs per SM
 }
 // Token slices of the dWr reduction: one wave of CTAs (three per SM for one
 // n-tile, two otherwise: the register budget), each slice a multiple of
@@ -800,11 +800,10 @@ extern "C" int moe_router_backward(const void* x, const void* w_r, const float* 
   dim3 gdw((unsigned)((H + 255) / 256), (unsigned)used, (unsigned)(((E + 7) / 8 + ntg - 1) / ntg));
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   int rc = MOE_OK;
-  switch (ntg) {
-    case 1: rc = launch_dw<1>(gdw, st, xb, dlogits, T, H, E, (int)slice, part); break;
-    case 2: rc = launch_dw<2>(gdw, st, xb, dlogits, T, H, E, (int)slice, part); break;
-    default: rc = launch_dw<4>(gdw, st, xb, dlogits, T, H, E, (int)slice, part); break;
-  }
+  if (ntg == 1)
+    rc = launch_dw<1>(gdw, st, xb, dlogits, T, H, E, (int)slice, part);
+  else
+    rc = launch_dw<2>(gdw, st, xb, dlogits, T, H, E, (int)slice, part);
   if (rc != MOE_OK) return rc;
   const long long HE = (long long)H * E;
   long long fb = (HE + 255) / 256;
