@@ -674,6 +674,21 @@ extern "C" int moe_grouped_gemm_mxfp8(int mode, const uint8_t* a, const uint8_t*
       b_rows % 128 || b_cols % 128 || a_rows >= (1LL << 31) || a_cols >= (1LL << 31) ||
       b_rows >= (1LL << 31) || b_cols >= (1LL << 31))
     return MOE_ERR_ARG;
+  // the mode's own shape rules, all checked before any CUDA call
+  if (mode == MOE_GEMM_FPROP) {
+    if (N < 128 || N % 128 || K < MX::BK || K % MX::BK || b_row_stride < 0 || b_k_stride < 0)
+      return MOE_ERR_ARG;
+    // every B row and K index that any expert touches must lie inside B
+    if ((E - 1) * b_row_stride + ((N + MX::BN - 1) / MX::BN) * MX::BN > b_rows + MX::BN / 2 ||
+        (E - 1) * b_k_stride + K > b_cols || K > a_cols)
+      return MOE_ERR_ARG;
+  } else if (mode == MOE_GEMM_WGRAD) {
+    if (M < MX::BM || M % MX::BM || N < MX::BN || N % MX::BN || M > a_rows || N > b_rows ||
+        a_cols != b_cols)
+      return MOE_ERR_ARG;
+  } else {
+    return MOE_ERR_ARG;
+  }
   MX::MxParams p{};
   p.offsets = offsets;
   p.E = E;
@@ -691,25 +706,14 @@ extern "C" int moe_grouped_gemm_mxfp8(int mode, const uint8_t* a, const uint8_t*
   if (!MX::u8_map(&ta, a, a_rows, a_cols) || !MX::u8_map(&tb, b, b_rows, b_cols)) return MOE_ERR_CUDA;
   cudaStream_t st = (cudaStream_t)stream;
   if (mode == MOE_GEMM_FPROP) {
-    if (N < 128 || N % 128 || K < MX::BK || K % MX::BK || b_row_stride < 0 || b_k_stride < 0)
-      return MOE_ERR_ARG;
-    // every B row and K index that any expert touches must lie inside B
-    if ((E - 1) * b_row_stride + ((N + MX::BN - 1) / MX::BN) * MX::BN > b_rows + MX::BN / 2 ||
-        (E - 1) * b_k_stride + K > b_cols || K > a_cols)
-      return MOE_ERR_ARG;
     p.b_row_stride = b_row_stride;
     p.b_k_stride = b_k_stride;
     long long bound = (a_rows / MX::BM + E) * (long long)((N + MX::BN - 1) / MX::BN);
     return MX::launch<FPROP, EPI_STORE>(ta, tb, tb, p, bound, st);
   }
-  if (mode == MOE_GEMM_WGRAD) {
-    if (M < MX::BM || M % MX::BM || N < MX::BN || N % MX::BN || M > a_rows || N > b_rows || a_cols != b_cols)
-      return MOE_ERR_ARG;
-    p.c_group_stride = (long long)M * N;
-    long long bound = (long long)E * (M / MX::BM) * (N / MX::BN);
-    return MX::launch<WGRAD, EPI_STORE>(ta, tb, tb, p, bound, st);
-  }
-  return MOE_ERR_ARG;
+  p.c_group_stride = (long long)M * N;
+  long long bound = (long long)E * (M / MX::BM) * (N / MX::BN);
+  return MX::launch<WGRAD, EPI_STORE>(ta, tb, tb, p, bound, st);
 }
 
 extern "C" int moe_fc1_swiglu_mxfp8(const uint8_t* xq, const uint8_t* sx, long long rows, int H,

@@ -220,3 +220,73 @@ def test_binding_element_types_follow_the_header(host_binding):
     for call in wrong:
         with pytest.raises(B.MoeError, match="element type"):
             call()
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="passes made-up device addresses: only on a host with no GPU")
+def test_bad_arguments_return_arg_error_before_any_cuda_call(libmoe):
+    """Each entry point returns MOE_ERR_ARG (1) for a bad size, count, mode or
+    alignment, with non-null buffers, before any CUDA call. On a host without
+    a GPU a missed check would show as MOE_ERR_CUDA (3), since every CUDA call
+    fails there; nothing can be launched."""
+    import ctypes as C
+    from mixture_experts_expert_sort_b300 import binding as B
+    L = B.lib()
+    P = 0x100000  # a made-up, 256-byte aligned address: never dereferenced here
+    cases = {
+        "route T < 0": ("moe_route", P, -1, 8, 2, P, P, None),
+        "route E = 0": ("moe_route", P, 16, 0, 1, P, P, None),
+        "route E > 256": ("moe_route", P, 16, 257, 2, P, P, None),
+        "route k > E": ("moe_route", P, 16, 4, 5, P, P, None),
+        "route k > 8": ("moe_route", P, 16, 64, 9, P, P, None),
+        "route_backward n_part = 0": ("moe_route_backward", P, 1, 0, P, P, P, 16, 8, 2, P, None),
+        "route_backward ld < n_part": ("moe_route_backward", P, 1, 2, P, P, P, 16, 8, 2, P, None),
+        "plan align = 0": ("moe_permute_plan", P, 16, 8, 2, 0, P, P, P, P, 4096, P, 1 << 20,
+                           None),
+        "plan workspace too small": ("moe_permute_plan", P, 16, 8, 2, 128, P, P, P, P, 4096, P,
+                                     0, None),
+        "plan src too short": ("moe_permute_plan", P, 16, 8, 2, 128, P, P, P, P, 1, P, 1 << 20,
+                               None),
+        "plan_static E = 0": ("moe_permute_plan_static", P, 16, 0, 1, 128, P, P, P, P, 4096,
+                              None),
+        "permute H % 8": ("moe_permute", P, P, P, P, P, 16, 12, 8, 2, P, P, None),
+        "permute x misaligned": ("moe_permute", P + 8, P, P, P, P, 16, 128, 8, 2, P, P, None),
+        "unpermute H % 8": ("moe_unpermute", P, P, P, 16, 12, 2, P, None),
+        "quantize no direction": ("mxfp8_quantize", P, 128, 128, 128, None, 1, 0, P, P, P, P,
+                                  None),
+        "quantize ld < cols": ("mxfp8_quantize", P, 128, 256, 128, None, 1, 3, P, P, P, P, None),
+        "quantize cols % 128": ("mxfp8_quantize", P, 128, 96, 96, None, 1, 3, P, P, P, P, None),
+        "quantize src_div = 0": ("mxfp8_quantize", P, 128, 128, 128, P, 0, 3, P, P, P, P, None),
+        "gemm_bf16 mode": ("moe_grouped_gemm_bf16", 7, P, P, 0, P, 4, 512, 0, 256, 128, P, None),
+        "gemm_bf16 b_layout": ("moe_grouped_gemm_bf16", 0, P, P, 3, P, 4, 512, 0, 256, 128, P,
+                               None),
+        "gemm_bf16 E = 0": ("moe_grouped_gemm_bf16", 0, P, P, 0, P, 0, 512, 0, 256, 128, P, None),
+        "fc1_swiglu_bf16 F = 0": ("moe_fc1_swiglu_bf16", P, P, P, P, 4, 512, 128, 0, P, P, None),
+        "fc2_dgrad_bf16 E = 0": ("moe_fc2_dgrad_swiglu_bwd_bf16", P, P, P, P, P, 0, 512, 128,
+                                 256, P, P, None),
+        "gemm_mxfp8 mode": ("moe_grouped_gemm_mxfp8", 5, P, P, 512, 128, P, P, 256, 512, 0, 0, P,
+                            4, 0, 256, 128, P, None),
+        "gemm_mxfp8 FPROP N % 128": ("moe_grouped_gemm_mxfp8", 0, P, P, 512, 128, P, P, 256, 512,
+                                     0, 128, P, 4, 0, 100, 128, P, None),
+        "gemm_mxfp8 FPROP B too short": ("moe_grouped_gemm_mxfp8", 0, P, P, 512, 128, P, P, 256,
+                                         512, 0, 256, P, 4, 0, 256, 128, P, None),
+        "gemm_mxfp8 WGRAD K mismatch": ("moe_grouped_gemm_mxfp8", 1, P, P, 256, 512, P, P, 256,
+                                        384, 0, 0, P, 4, 128, 128, 0, P, None),
+        "fc1_swiglu_mxfp8 rows % 128": ("moe_fc1_swiglu_mxfp8", P, P, 100, 128, P, P, P, P, 4,
+                                        256, P, P, P, P, P, None),
+        "fc2_dgrad_mxfp8 F % 128": ("moe_fc2_dgrad_swiglu_bwd_mxfp8", P, P, 512, 128, P, P, P, P,
+                                    P, 4, 100, P, P, P, P, P, None),
+        "router_forward workspace": ("moe_router_forward", P, P, 64, 128, 8, 2, P, P, P, P, P, 0,
+                                     None),
+        "router_forward k > E": ("moe_router_forward", P, P, 64, 128, 2, 3, P, P, P, P, P,
+                                 1 << 24, None),
+        "router_backward workspace": ("moe_router_backward", P, P, P, P, P, 0.01, 64, 128, 8, P,
+                                      None, P, P, P, 0, None),
+    }
+    for what, (name, *args) in cases.items():
+        assert getattr(L, name)(*args) == 1, what
+    good = B.layer_config(256, 128, 256, 4, 2)
+    bad = B.layer_config(256, 100, 256, 4, 2)
+    assert L.moe_layer_forward(C.byref(bad), P, P, P, P, P, P, 1 << 30, None) == 1
+    assert L.moe_layer_forward(C.byref(good), P, P, P, P, P, P, 16, None) == 1
+    assert L.moe_layer_backward(C.byref(good), P, P, P, P, P, P, P, P, 16, None) == 1
