@@ -149,3 +149,15 @@ def test_mxfp4_conversion_bytes_are_the_oracle_outputs():
     x = _np(I.make_x(wl))
     row = _mx8_bytes(*O.mx_quantize(np.repeat(x, wl.k, axis=0), axis=1))
     assert work["quant_x"] == ("bytes", pytest.approx(2 * x.size + row))
+
+
+def test_peaks_measured_file_else_fallback(monkeypatch, tmp_path):
+    """Roofline denominators: the measured peaks file when present (the
+    sustained rate defaults to the burst one), else the fallback figures
+    6.4 TB/s, 1.8 PFLOP/s bf16 burst and 1.4 sustained, labelled as such."""
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_peaks() == {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0,
+                                  "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+    (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 6000.5, "bf16_tflops": 1700.0}')
+    assert bench.load_peaks() == {"hbm_gbs": 6000.5, "bf16_tflops": 1700.0,
+                                  "bf16_tflops_sustained": 1700.0, "source": "measured"}
