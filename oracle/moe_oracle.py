@@ -44,12 +44,16 @@ Readings where the sources are silent (each is repeated in the design notes):
   along tokens inside an expert group, for wgrad); intermediate activations
   are rounded to float32 before they are quantised; the elementwise
   backward is straight-through;
-* in MXFP8 mode the SwiGLU backward works from the gate/up values that the
-  forward saved in BF16: [EMT §Challenge 3] has each low-precision GEMM's
-  result converted back to the 16-bit format, and the values this step
-  produces decide quantised codes, so the oracle takes that decision from
-  the same BF16 inputs as the kernel. The forward SwiGLU consumes the GEMM
-  result unrounded (the fused path folds the conversion into the epilogue);
+* the SwiGLU backward works from the gate/up values that the forward saved
+  in BF16 (save_bf16=True, the default, in every precision): [EMT §Challenge
+  3] trains with 16-bit activations and converts each low-precision GEMM's
+  result back to the 16-bit format. Two results depend on that rounding far
+  more than the tolerance: in MXFP8 mode the values this step produces decide
+  quantised codes, and dlogits = w (dp - sum w dp) cancels when a token's dp
+  values are close (for a single token the rounding alone moves it by 6%).
+  The forward SwiGLU consumes the GEMM result unrounded (the fused path folds
+  the conversion into the epilogue). save_bf16=False gives the exact
+  chain-rule gradient that the finite-difference pin checks;
 * in the MXFP8 mode with MXFP4 activations (mx == "act4") the wgrad operands
   X and H are the FP8 -> FP4 -> column-wise FP4 chain of their row-wise MXFP8
   copies (act4_cols_in_groups; the MXFP4 readings are in mxfp4_oracle.py);
@@ -400,9 +404,10 @@ def to_bf16(a):
     return r.view(np.float32).astype(f64)
 
 
-def saved_gate_up(g, u, mx):
-    """Gate and up values the backward reads: BF16-saved in MXFP8 mode."""
-    return (to_bf16(g), to_bf16(u)) if mx else (g, u)
+def saved_gate_up(g, u, save_bf16):
+    """Gate and up values the backward reads: their BF16 copies when the
+    forward saves them in BF16, else the exact values."""
+    return (to_bf16(g), to_bf16(u)) if save_bf16 else (g, u)
 
 
 # ---------------------------------------------------------------------------
@@ -465,7 +470,7 @@ def expert_forward(xe, p, W1e, W2e, mx=False):
     return y2, {"g": g, "u": u, "h": h}
 
 
-def expert_backward(xe, p, W1e, W2e, dy2, saved, mx=False):
+def expert_backward(xe, p, W1e, W2e, dy2, saved, mx=False, save_bf16=True):
     """Chain rule through one expert.
 
     dH = dY2 @ W2^T; a = silu(g)*u; dA = dH*p; dp = sum_f dH*a;
@@ -473,7 +478,7 @@ def expert_backward(xe, p, W1e, W2e, dy2, saved, mx=False):
     dW2 = H^T @ dY2; dXp = dY1 @ W1^T; dW1 = Xp^T @ dY1.
     Returns (dxp [n, H], dp [n], dW1e [H, 2F], dW2e [F, H]).
     """
-    g, u = saved_gate_up(saved["g"], saved["u"], mx)
+    g, u = saved_gate_up(saved["g"], saved["u"], save_bf16)
     h = saved["h"]
     p = np.asarray(p, dtype=f64)[:, None]
     dy2 = np.asarray(dy2, dtype=f64)
@@ -506,10 +511,11 @@ def expert_backward(xe, p, W1e, W2e, dy2, saved, mx=False):
 # The whole layer, written as the per-expert loop of [EMT §Challenge 1]
 # ---------------------------------------------------------------------------
 
-def layer_forward(x, logits, W1, W2, k, mx=False):
+def layer_forward(x, logits, W1, W2, k, mx=False, save_bf16=True):
     """out[t] = sum over the experts e chosen by t of the weighted expert MLP.
 
-    Returns a dict with out [T, H], idx, w and the per-expert saved state.
+    Returns a dict with out [T, H], idx, w and the per-expert saved state
+    (the backward reads gate/up through their BF16 copies when save_bf16).
     """
     x = np.asarray(x, dtype=f64)
     idx, w = route(logits, k)
@@ -523,7 +529,8 @@ def layer_forward(x, logits, W1, W2, k, mx=False):
         y2, s = expert_forward(x[tok], p, W1[e], W2[e], mx)
         np.add.at(out, tok, y2)
         saved.append((tok, slot, s))
-    return {"out": out, "idx": idx, "w": w, "saved": saved, "k": k, "mx": mx}
+    return {"out": out, "idx": idx, "w": w, "saved": saved, "k": k, "mx": mx,
+            "save_bf16": save_bf16}
 
 
 def layer_backward(fwd, x, W1, W2, dout):
@@ -540,14 +547,14 @@ def layer_backward(fwd, x, W1, W2, dout):
     for e in range(E):
         tok, slot, s = fwd["saved"][e]
         dxp, dpe, dW1[e], dW2[e] = expert_backward(
-            x[tok], w[tok, slot], W1[e], W2[e], dout[tok], s, mx)
+            x[tok], w[tok, slot], W1[e], W2[e], dout[tok], s, mx, fwd["save_bf16"])
         np.add.at(dX, tok, dxp)
         dp[tok, slot] = dpe
     dlogits = route_backward(dp, w, idx, E)
     return {"dX": dX, "dW1": dW1, "dW2": dW2, "dlogits": dlogits, "dp": dp}
 
 
-def layer_fwd_bwd_expert_stream(x, logits, W1, W2, dout, k, mx=False):
+def layer_fwd_bwd_expert_stream(x, logits, W1, W2, dout, k, mx=False, save_bf16=True):
     """The same per-expert loop, yielding each expert's results in turn.
 
     Yields (e, tok, slot, y2, dxp, dp, dW1e, dW2e) and holds only one
@@ -561,7 +568,8 @@ def layer_fwd_bwd_expert_stream(x, logits, W1, W2, dout, k, mx=False):
         tok, slot = expert_rows(idx, e)
         p = w[tok, slot]
         y2, s = expert_forward(x[tok], p, W1[e], W2[e], mx)
-        dxp, dpe, dW1e, dW2e = expert_backward(x[tok], p, W1[e], W2[e], dout[tok], s, mx)
+        dxp, dpe, dW1e, dW2e = expert_backward(x[tok], p, W1[e], W2[e], dout[tok], s, mx,
+                                               save_bf16)
         yield e, tok, slot, y2, dxp, dpe, dW1e, dW2e
 
 
@@ -583,7 +591,7 @@ def map_experts(fn, E):
     with ThreadPoolExecutor(max_workers=workers) as ex:
         return list(ex.map(fn, range(E)))
 
-def sampled_token_outputs(x, logits, W1, W2, dout, k, tokens, mx=False):
+def sampled_token_outputs(x, logits, W1, W2, dout, k, tokens, mx=False, save_bf16=True):
     """out, dX and dlogits for the given tokens only.
 
     Each of these depends only on the token's own k routed rows (every
@@ -611,7 +619,7 @@ def sampled_token_outputs(x, logits, W1, W2, dout, k, tokens, mx=False):
         # Row-local backward: dY1 row quantisation and the dgrads need only
         # the row itself; the wgrad outputs of expert_backward are discarded.
         dy2 = dout[tokens[ti]].astype(f64)
-        g, u = saved_gate_up(s["g"], s["u"], mx)
+        g, u = saved_gate_up(s["g"], s["u"], save_bf16)
         dy2_row = mx_qdq(dy2, axis=1) if mx else dy2
         dh = dy2_row @ _w2_dgrad(W2[e], mx).T
         a = silu(g) * u
@@ -633,7 +641,7 @@ def sampled_token_outputs(x, logits, W1, W2, dout, k, tokens, mx=False):
     return {"out": out, "dX": dX, "dlogits": dlogits, "idx": idx_all, "w": w_all}
 
 
-def sampled_weight_grads(x, logits, W1, W2, dout, k, fcols, mx=False):
+def sampled_weight_grads(x, logits, W1, W2, dout, k, fcols, mx=False, save_bf16=True):
     """dW1[:, :, c], dW1[:, :, F+c] and dW2[:, c, :] for the FFN columns c in fcols.
 
     fcols must be whole 32-aligned blocks of [0, F), so every row-wise block
@@ -670,7 +678,7 @@ def sampled_weight_grads(x, logits, W1, W2, dout, k, fcols, mx=False):
         y1 = xin @ W1f
         g, u = y1[:, :nc], y1[:, nc:]
         h = silu(g) * u * p
-        g, u = saved_gate_up(g, u, mx)
+        g, u = saved_gate_up(g, u, save_bf16)
         # dH columns c: dY2 (row-quantised along H) times W2 rows c (quantised along H).
         dy2 = dout[tok].astype(f64)
         dy2_row = mx_qdq(dy2, axis=1) if mx else dy2

@@ -3,7 +3,10 @@ oracle's per-expert loop, on the seeded synthetic workloads.
 
 Integer results (routing indices, counts, offsets, dest, src) must match
 bit-exactly. Float results must have relative Frobenius error <= 5e-3 and
-max-abs error <= 1e-2 * max|ref| (the BF16 tolerance the layer is held to).
+max-abs error <= 1e-2 * max|ref| (the BF16 tolerance the layer is held to),
+on every shape. The oracle's backward reads gate/up through their bf16
+copies, as the layer saves them; dlogits = w (dp - sum w dp) would otherwise
+be dominated by that rounding wherever a token's dp values nearly cancel.
 """
 import numpy as np
 import pytest
@@ -39,22 +42,7 @@ def _check(name, got, ref):
     assert e1 <= TOL_FRO and e2 <= TOL_MAX, (name, e1, e2)
 
 
-def _check_dlogits(got, ref, dp_ref, strict):
-    """dlogits[t, e_j] = w_j (dp_j - sum_i w_i dp_i) is a difference of the
-    dL/dw values dp, which the BF16 path computes from the bf16-rounded saved
-    gate/up activations. With many tokens the Frobenius criterion holds; for
-    a handful of tokens the cancellation can leave one value with a larger
-    relative error, so the edge cases may instead bound the absolute error by
-    the bf16 rounding of dp: max |d - d_ref| <= 4e-3 * max |dp|."""
-    e1, e2 = rel_fro(got, ref), max_abs_rel(got, ref)
-    if e1 <= TOL_FRO and e2 <= TOL_MAX:
-        return
-    assert not strict, ("dlogits", e1, e2)
-    bound = 4e-3 * np.max(np.abs(dp_ref))
-    assert np.max(np.abs(got - ref)) <= bound, ("dlogits", e1, e2, bound)
-
-
-def _full_parity(wl, inp, strict_dlogits=True):
+def _full_parity(wl, inp):
     L, g = _run(wl, inp)
     x, lg = f64(inp["x"]), f64(inp["logits"])
     w1, w2, dout = f64(inp["w1"]), f64(inp["w2"]), f64(inp["dout"])
@@ -72,7 +60,7 @@ def _full_parity(wl, inp, strict_dlogits=True):
     _check("dX", f64(g["dX"]), bwd["dX"])
     _check("dW1", f64(g["dW1"]), bwd["dW1"])
     _check("dW2", f64(g["dW2"]), bwd["dW2"])
-    _check_dlogits(f64(g["dlogits"]), bwd["dlogits"], bwd["dp"], strict_dlogits)
+    _check("dlogits", f64(g["dlogits"]), bwd["dlogits"])
 
 
 def test_tiny_workload_full_parity():
@@ -93,7 +81,7 @@ EDGE = [
 @pytest.mark.parametrize("T,H,F,E,k,zs,ze", EDGE)
 def test_edge_workloads_full_parity(T, H, F, E, k, zs, ze):
     wl = I.Workload("edge", T, H, F, E, k, "bf16", 2000 + T + E, zipf_s=zs, zero_experts=ze)
-    _full_parity(wl, I.make_all(wl), strict_dlogits=T >= 100)
+    _full_parity(wl, I.make_all(wl))
 
 
 def test_deterministic_bytes():

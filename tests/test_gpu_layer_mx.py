@@ -117,19 +117,6 @@ def _check_plan(L, wl, idx_ref):
     assert np.all(gsrc[len(src):] == -1)
 
 
-def _check_dlogits(got, ref, dp_ref, strict):
-    """As in the BF16 layer test: dlogits is a difference of dL/dw values that
-    the GPU computes from the bf16-saved gate/up activations; for a handful of
-    tokens one value may carry a larger relative error, so edge cases may
-    instead bound the absolute error by the bf16 rounding of dp."""
-    e = rel_fro(got, ref)
-    if e <= TOL_MX:
-        return
-    assert not strict, ("dlogits", e)
-    bound = 4e-3 * np.max(np.abs(dp_ref))
-    assert np.max(np.abs(got - ref)) <= bound, ("dlogits", e, bound)
-
-
 EDGE = [
     # T, H, F, E, k, zipf_s, zero_experts, outlier_frac
     (256, 256, 256, 4, 2, 0.0, 0, 0.0),     # a tiny Mixtral-like layer
@@ -158,7 +145,7 @@ def test_mx_layer_full_parity(T, H, F, E, k, zs, ze, of):
     _check("dX", f64(g["dX"]), bwd["dX"])
     _check("dW1", f64(g["dW1"]), bwd["dW1"])
     _check("dW2", f64(g["dW2"]), bwd["dW2"])
-    _check_dlogits(f64(g["dlogits"]), bwd["dlogits"], bwd["dp"], strict=T >= 100)
+    _check("dlogits", f64(g["dlogits"]), bwd["dlogits"])
 
 
 def test_mx_layer_deterministic():
@@ -240,7 +227,7 @@ def test_act4_layer_full_parity(T, H, F, E, k, zs, ze, of):
     _check("dX", f64(g["dX"]), bwd["dX"])
     _check("dW1", f64(g["dW1"]), bwd["dW1"])
     _check("dW2", f64(g["dW2"]), bwd["dW2"])
-    _check_dlogits(f64(g["dlogits"]), bwd["dlogits"], bwd["dp"], strict=T >= 100)
+    _check("dlogits", f64(g["dlogits"]), bwd["dlogits"])
     # the MXFP4 chain is what the weight gradients saw: the plain MXFP8
     # oracle differs from it by more than the tolerance on dW1
     ref8 = O.layer_backward(O.layer_forward(x, lg, w1, w2, wl.k, mx=True), x, w1, w2, dout)

@@ -98,13 +98,17 @@ def _sig(z):
     return 1.0 / (1.0 + np.exp(-z))
 
 
-def reference_layer(x, lg, W1, W2, dout, k, act4=False):
-    """The MXFP8 layer with every quantised product a block_scaled_gemm.
+def reference_layer(x, lg, W1, W2, dout, k, act4=False, mx=True, save_bf16=True):
+    """The MXFP8 layer with every quantised product a block_scaled_gemm (or,
+    with mx=False, the BF16-mode layer with plain products).
 
     Readings shared with the oracle (stated in its header): activations are
     rounded to fp32 before they are quantised; the SwiGLU backward reads the
-    gate/up values saved in bf16; the elementwise backward is straight-through.
+    gate/up values saved in bf16 (unless save_bf16 is False); the elementwise
+    backward is straight-through.
     """
+    gemm = block_scaled_gemm if mx else (lambda A, B: np.asarray(A) @ np.asarray(B))
+    rnd = _f32 if mx else (lambda a: a)
     T, H = x.shape
     E, _, F2 = W1.shape
     F = F2 // 2
@@ -123,18 +127,18 @@ def reference_layer(x, lg, W1, W2, dout, k, act4=False):
         p = w[tok, slot][:, None]
         xe, dye = x[tok], dout[tok]
         # forward: FC1 contracts H, FC2 contracts F
-        y1 = block_scaled_gemm(xe, W1[e])
+        y1 = gemm(xe, W1[e])
         g, u = y1[:, :F], y1[:, F:]
-        h = _f32(g * _sig(g) * u * p)
-        y2 = block_scaled_gemm(h, W2[e])
+        h = rnd(g * _sig(g) * u * p)
+        y2 = gemm(h, W2[e])
         # backward: FC2 dgrad contracts H, FC1 dgrad contracts 2F, wgrads contract tokens
-        gb, ub = _bf16(g), _bf16(u)
-        dh = block_scaled_gemm(dye, W2[e].T)
+        gb, ub = (_bf16(g), _bf16(u)) if save_bf16 else (g, u)
+        dh = gemm(dye, W2[e].T)
         sg = _sig(gb)
         dA = dh * p
         dpe = (dh * gb * sg * ub).sum(axis=1)
-        dy1 = _f32(np.concatenate([dA * ub * sg * (1.0 + gb * (1.0 - sg)), dA * gb * sg], axis=1))
-        dxp = block_scaled_gemm(dy1, W1[e].T)
+        dy1 = rnd(np.concatenate([dA * ub * sg * (1.0 + gb * (1.0 - sg)), dA * gb * sg], axis=1))
+        dxp = gemm(dy1, W1[e].T)
         n = len(rows)
         if act4:
             hT = act4_operand(h.T, k_axis=1)  # [F, n_pad]
@@ -142,8 +146,8 @@ def reference_layer(x, lg, W1, W2, dout, k, act4=False):
             dW2[e] = block_scaled_gemm(hT, _pad_rows(dye))
             dW1[e] = block_scaled_gemm(xT, _pad_rows(dy1))
         else:
-            dW2[e] = block_scaled_gemm(h.T, dye)
-            dW1[e] = block_scaled_gemm(xe.T, dy1)
+            dW2[e] = gemm(h.T, dye)
+            dW1[e] = gemm(xe.T, dy1)
         for i in range(n):
             out[tok[i]] += y2[i]
             dX[tok[i]] += dxp[i]
@@ -187,8 +191,8 @@ def _rel(a, b):
     return float(np.linalg.norm(a - b) / (nb if nb > 0 else 1.0))
 
 
-def _oracle(x, lg, W1, W2, dout, k, mx):
-    f = O.layer_forward(x, lg, W1, W2, k, mx=mx)
+def _oracle(x, lg, W1, W2, dout, k, mx, save_bf16=True):
+    f = O.layer_forward(x, lg, W1, W2, k, mx=mx, save_bf16=save_bf16)
     b = O.layer_backward(f, x, W1, W2, dout)
     return {"out": f["out"], **{n: b[n] for n in ("dX", "dW1", "dW2", "dlogits")}}
 
@@ -223,6 +227,20 @@ def test_oracle_act4_weight_grads_equal_block_scaled_reference(T, H, F, E, k, gs
     mx8 = _oracle(x, lg, W1, W2, dout, k, True)
     assert _rel(mx8["dW1"], ref["dW1"]) > 1e-3 and _rel(mx8["dW2"], ref["dW2"]) > 1e-3
     assert _rel(mx8["dX"], ref["dX"]) < TOL
+
+
+@pytest.mark.parametrize("save_bf16", [True, False])
+def test_oracle_bf16_layer_equals_reference(save_bf16):
+    """The BF16 mode: plain products, and the backward reads gate/up through
+    their bf16 copies (the library's cast) unless save_bf16 is False."""
+    T, H, F, E, k, gs = CASES[1]
+    x, lg, W1, W2, dout = _layer(45, T, H, F, E, k, gs)
+    ref = reference_layer(x, lg, W1, W2, dout, k, mx=False, save_bf16=save_bf16)
+    got = _oracle(x, lg, W1, W2, dout, k, False, save_bf16)
+    for n in ref:
+        assert _rel(got[n], ref[n]) < TOL, (n, _rel(got[n], ref[n]))
+    other = reference_layer(x, lg, W1, W2, dout, k, mx=False, save_bf16=not save_bf16)
+    assert _rel(got["dW1"], other["dW1"]) > 1e-4  # the rounding is visible
 
 
 # ------------------------------------------- planted wrong axes must be caught
