@@ -198,10 +198,13 @@ MOE_API int moe_permute_plan(const int32_t* idx, int T, int E, int k, int align,
  *   Limit: ceil(T*k / 1024) * E <= MOE_PLAN_STATIC_SCRATCH_INTS, else
  *   MOE_ERR_UNSUPPORTED and nothing is enqueued.
  *   The first call on each device looks up the array's device address (with
- *   that device current); make that first call before any stream capture.
- *   Every call shares the array: calls that overlap on the GPU (other
- *   streams, threads) race and must be serialised by the caller. Each call
- *   overwrites the scratch it reads, so nothing carries over between calls.
+ *   that device current) and keeps it; make that first call before any
+ *   stream capture. The kept address does not survive cudaDeviceReset: do not
+ *   call this entry point again in a process that reset the device.
+ *   Each device holds its own copy of the array. Calls on the same device
+ *   share it: calls that overlap on that GPU (other streams, threads) race
+ *   and must be serialised by the caller. Each call overwrites the scratch it
+ *   reads, so nothing carries over between calls.
  */
 #define MOE_PLAN_STATIC_SCRATCH_INTS 262144
 MOE_API int moe_permute_plan_static(const int32_t* idx, int T, int E, int k, int align,

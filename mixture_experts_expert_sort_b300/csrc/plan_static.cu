@@ -9,10 +9,17 @@
 // moe_permute_plan and gives bit-identical results.
 //
 // The array lives for as long as the library is loaded, on every GPU that
-// loads it (1 MiB each). All calls share it: the plan overwrites every scratch
-// word it reads during the same call, so no clearing is needed between calls,
-// but calls that run at the same time on the GPU (different streams, threads
-// or devices' contexts sharing it) race and must be serialised by the caller.
+// loads it (1 MiB each; every device has its own copy). All calls on one
+// device share that device's copy: the plan overwrites every scratch word it
+// reads during the same call, so no clearing is needed between calls, but
+// calls on the same device that run at the same time on the GPU (different
+// streams or host threads) race and must be serialised by the caller. Calls
+// on different devices use different copies and do not race.
+//
+// The device address of the array is looked up by the first call on each
+// device and kept. A cudaDeviceReset destroys the module image it points
+// into, so after a reset this entry point must not be called again in the
+// same process.
 #include <mutex>
 
 #include "common.cuh"
