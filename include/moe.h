@@ -264,6 +264,19 @@ MOE_API int mxfp8_quantize(const void* in, long long rows, int cols, long long l
                    int src_div, int dirs, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
                    uint8_t* s_col, moe_stream_t stream);
 
+/* mxfp8_scales_to_canonical: the scales of an MXFP8 operand with MN rows and
+ * K columns, given in the tiled layout above, rewritten row-major:
+ * canon[r * (K/32) + c] = scale byte of row r and 32-column block c (the
+ * plain [MN, K/32] E8M0 array of the OCP MX format, one byte per block of
+ * 32 consecutive values, "Efficient MoE Training ...", §Challenge 2). For
+ * tests and for handing scales to other software; the GEMMs read only the
+ * tiled layout.
+ *   tiled: mn*kdim/32 bytes (in).  canon: mn*kdim/32 bytes (out); the two
+ *   must not overlap and both must be 4-byte aligned.
+ *   Requires mn % 128 == 0 and kdim % 128 == 0 (mn == 0 does nothing). */
+MOE_API int mxfp8_scales_to_canonical(const uint8_t* tiled, long long mn, int kdim,
+                                      uint8_t* canon, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * MXFP4 activation compression (the hgpu.org abstract on MXFP4 training of
  * MoE models on Hopper: activations are kept in MXFP4 while the GEMMs run in

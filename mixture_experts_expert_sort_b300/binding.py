@@ -41,6 +41,7 @@ SIGNATURES = {
     "moe_permute": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _p, _p, _p]),
     "moe_unpermute": (_i, [_p, _p, _p, _i, _i, _i, _p, _p]),
     "mxfp8_quantize": (_i, [_p, _ll, _i, _ll, _p, _i, _i, _p, _p, _p, _p, _p]),
+    "mxfp8_scales_to_canonical": (_i, [_p, _ll, _i, _p, _p]),
     "mxfp4_from_mxfp8": (_i, [_p, _p, _ll, _i, _p, _p, _p]),
     "mxfp8_from_mxfp4": (_i, [_p, _p, _ll, _i, _p, _p, _p]),
     "mxfp4_rowwise_to_colwise": (_i, [_p, _p, _ll, _i, _p, _p, _p]),
@@ -323,6 +324,15 @@ def mxfp8_quantize(x, dirs=QUANT_ROWWISE | QUANT_COLWISE, rows=None, src=None, s
                                 dirs, ptr(out.get("q_row"), U8), ptr(out.get("s_row"), U8),
                                 ptr(out.get("q_col"), U8), ptr(out.get("s_col"), U8),
                                 stream_handle(stream)), "mxfp8_quantize")
+    return out
+
+
+def mxfp8_scales_to_canonical(s_tiled, mn, kdim, stream=None, out=None):
+    """Tiled scales of an [mn, kdim] MXFP8 operand -> row-major [mn, kdim/32] bytes."""
+    out = out if out is not None else torch.empty((mn, kdim // 32), dtype=torch.uint8,
+                                                  device=s_tiled.device)
+    _check(lib().mxfp8_scales_to_canonical(ptr(s_tiled, U8), mn, kdim, ptr(out, U8),
+                                           stream_handle(stream)), "mxfp8_scales_to_canonical")
     return out
 
 

@@ -238,10 +238,46 @@ __global__ void __launch_bounds__(kQThreads)
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
+// Tiled scales -> row-major [mn, kdim/32]. The four scales of row r and
+// 32-column blocks 4j .. 4j+3 are one aligned 32-bit word in both layouts, so
+// each thread moves one word: tiled word (tile (r/128, j), lane r % 32,
+// quarter (r % 128) / 32) to row-major word r * (kdim/128) + j. Consecutive
+// threads take consecutive output words (coalesced stores; the loads of a
+// warp fall in one or two 512-byte tiles).
+__global__ void __launch_bounds__(256)
+    mx_scales_canonical_kernel(const uint32_t* __restrict__ tiled, long long mn, int kt,
+                               uint32_t* __restrict__ canon) {
+  const long long words = mn * kt;
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < words; i += gridDim.x * 256LL) {
+    const long long r = i / kt;
+    const int j = (int)(i - r * kt);
+    const int rr = (int)(r & 127);
+    canon[i] = tiled[((r >> 7) * kt + j) * 128 + (rr & 31) * 4 + (rr >> 5)];
+  }
+}
+
 }  // namespace
 }  // namespace moe
 
 using namespace moe;
+
+extern "C" int mxfp8_scales_to_canonical(const uint8_t* tiled, long long mn, int kdim,
+                                         uint8_t* canon, moe_stream_t stream) {
+  if (mn < 0 || mn % 128 || kdim <= 0 || kdim % 128 || mn >= (1LL << 40)) return MOE_ERR_ARG;
+  if (mn == 0) return MOE_OK;
+  if (!tiled || !canon || (reinterpret_cast<uintptr_t>(tiled) & 3u) ||
+      (reinterpret_cast<uintptr_t>(canon) & 3u))
+    return MOE_ERR_ARG;
+  const long long bytes = mn * (kdim / 32);
+  const uintptr_t a = reinterpret_cast<uintptr_t>(tiled), c = reinterpret_cast<uintptr_t>(canon);
+  if (a < c + (uintptr_t)bytes && c < a + (uintptr_t)bytes) return MOE_ERR_ARG;  // overlap
+  const long long words = bytes / 4;
+  long long blocks = (words + 255) / 256;
+  if (blocks > 148 * 8) blocks = 148 * 8;
+  mx_scales_canonical_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
+      reinterpret_cast<const uint32_t*>(tiled), mn, kdim / 128, reinterpret_cast<uint32_t*>(canon));
+  return launch_status();
+}
 
 extern "C" int mxfp8_quantize(const void* in, long long rows, int cols, long long ld,
                               const int32_t* src, int src_div, int dirs, uint8_t* q_row,

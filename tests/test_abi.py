@@ -184,6 +184,7 @@ def test_binding_element_types_follow_the_header(host_binding):
     B.moe_unpermute(bf(rows, H), i32(R), T, k, w=f32(T, k))
     B.mxfp8_quantize(bf(T, H), rows=rows, src=i32(rows), src_div=k)
     B.mxfp8_quantize(bf(T, 2 * H)[:, :H])  # strided rows: the leading dimension is passed
+    B.mxfp8_scales_to_canonical(u8(rows * H // 32), rows, H)
     B.mxfp4_from_mxfp8(u8(rows, H), u8(rows * H // 32))
     B.mxfp8_from_mxfp4(u8(rows, H // 2), u8(rows * H // 32))
     B.mxfp4_rowwise_to_colwise(u8(rows, H // 2), u8(rows * H // 32))
@@ -209,6 +210,7 @@ def test_binding_element_types_follow_the_header(host_binding):
         lambda: B.moe_permute_plan(torch.zeros(T, k, dtype=torch.int64), E, 128),
         lambda: B.moe_permute(f32(T, H), i32(R), off, i32(E), k, rows),  # x is bf16
         lambda: B.mxfp8_quantize(f32(T, H)),
+        lambda: B.mxfp8_scales_to_canonical(i32(rows * H // 128), rows, H),
         lambda: B.mxfp4_from_mxfp8(i32(rows, H // 4), u8(rows * H // 32)),
         lambda: B.moe_grouped_gemm_bf16(B.GEMM_FPROP, bf(rows, H), bf(E, H, F), off.long()),
         lambda: B.moe_fc1_swiglu_bf16(bf(rows, H), bf(E, H, 2 * F), off, bf(rows)),
@@ -257,6 +259,11 @@ def test_bad_arguments_return_arg_error_before_any_cuda_call(libmoe):
         "quantize ld < cols": ("mxfp8_quantize", P, 128, 256, 128, None, 1, 3, P, P, P, P, None),
         "quantize cols % 128": ("mxfp8_quantize", P, 128, 96, 96, None, 1, 3, P, P, P, P, None),
         "quantize src_div = 0": ("mxfp8_quantize", P, 128, 128, 128, P, 0, 3, P, P, P, P, None),
+        "canonical mn % 128": ("mxfp8_scales_to_canonical", P, 100, 128, P + (1 << 20), None),
+        "canonical kdim % 128": ("mxfp8_scales_to_canonical", P, 128, 96, P + (1 << 20), None),
+        "canonical overlap": ("mxfp8_scales_to_canonical", P, 128, 128, P + 64, None),
+        "canonical misaligned": ("mxfp8_scales_to_canonical", P + 2, 128, 128, P + (1 << 20),
+                                 None),
         "gemm_bf16 mode": ("moe_grouped_gemm_bf16", 7, P, P, 0, P, 4, 512, 0, 256, 128, P, None),
         "gemm_bf16 b_layout": ("moe_grouped_gemm_bf16", 0, P, P, 3, P, 4, 512, 0, 256, 128, P,
                                None),

@@ -135,6 +135,19 @@ def test_mxfp8_quantize_both_directions(rows, cols):
     np.testing.assert_array_equal(scales_tiled_to_rowmajor(u8(q["s_col"]), cols, rows), s_col.T)
 
 
+@pytest.mark.parametrize("rows,cols", [(128, 128), (384, 640)])
+def test_mxfp8_scales_to_canonical(rows, cols):
+    """The device conversion of both scale copies to row-major bytes equals
+    the oracle's scales (row-wise [rows, cols/32]; column-wise [cols, rows/32])."""
+    x = _quant_input(rows, cols, 11 * rows + cols)
+    q = B().mxfp8_quantize(x.to(DEV))
+    _, s_row = O.mx_quantize(f64(x), axis=1)
+    _, s_col = O.mx_quantize(f64(x), axis=0)
+    np.testing.assert_array_equal(u8(B().mxfp8_scales_to_canonical(q["s_row"], rows, cols)), s_row)
+    np.testing.assert_array_equal(u8(B().mxfp8_scales_to_canonical(q["s_col"], cols, rows)),
+                                  s_col.T)
+
+
 def test_mxfp8_quantize_nonfinite_block():
     x = _quant_input(128, 128, 3, special=False)
     x[2, 40] = float("inf")
