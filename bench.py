@@ -5,9 +5,19 @@ scaled SwiGLU, FC2, combine, and the full backward) over one batch of T
 tokens, through the libmoe C ABI.
 
 Prints ONE JSON line (rank 0). Default: 1 GPU, the Mixtral-8x7B expert-layer
-workload in BF16 (T=8192, H=4096, F=14336, E=8, top-2).
+shape in MXFP8 (T=16384, H=4096, F=14336, E=8, top-2). The other workloads
+(tiny, Mixtral BF16, MXFP8 with MXFP4-carried activations, fine-grained
+skewed, long) are measured the same way in the same run and reported under
+"workloads" in that line (--configs none skips them).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--configs all|none|a,b]
+                  [--impl ours|reference]
+
+Timing: W untimed steps, then K steps between CUDA events on the launching
+stream; per-kernel times are means over the K steps (the statistic of
+ms_per_step). Roofline denominators: the measured BF16 burst rate (times 2,
+the nominal dense MXFP8/BF16 ratio, for MXFP8 GEMMs) and the measured HBM
+copy bandwidth.
 
 Multi-GPU (launched with torch.distributed.run): each rank runs its own
 T-token batch (the layer is data-parallel over tokens; no collective is on
@@ -42,10 +52,10 @@ def load_peaks():
             pk = json.load(f)
         return {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"],
                 "bf16_tflops_sustained": pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
-                "source": "measured"}
+                "sm_max_mhz": pk.get("sm_max_mhz", 2032.0), "source": "measured"}
     except Exception:
         return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
-                "source": "fallback"}
+                "sm_max_mhz": 2032.0, "source": "fallback"}
 
 
 # ------------------------------------------------------------------ clocks
@@ -333,29 +343,40 @@ def kernel_work(wl):
 _ORACLE_INPUTS = {}
 
 
-def _oracle_inputs(wl, t_slice):
-    key = (wl.name, t_slice)
-    if key not in _ORACLE_INPUTS:
-        inp = I.make_all(wl.with_tokens(t_slice))
-        _ORACLE_INPUTS[key] = (inp["x"].float().numpy(), inp["logits"].numpy(),
-                               inp["w1"].float().numpy(), inp["w2"].float().numpy(),
-                               inp["dout"].float().numpy())
-    return _ORACLE_INPUTS[key]
+def _oracle_inputs(wl):
+    """The workload's inputs on the host, routed once (before any clock starts)."""
+    if wl.name not in _ORACLE_INPUTS:
+        from oracle import moe_oracle as O
+        inp = I.make_all(wl)
+        lg = inp["logits"].numpy()
+        idx, w = O.route(lg, wl.k)
+        _ORACLE_INPUTS[wl.name] = {
+            "x": inp["x"].float().numpy(), "w1": inp["w1"].float().numpy(),
+            "w2": inp["w2"].float().numpy(), "dout": inp["dout"].float().numpy(), "w": w,
+            "rows": [O.expert_rows(idx, e) for e in range(wl.E)]}
+    return _ORACLE_INPUTS[wl.name]
 
 
-def oracle_sample_time(wl, t_slice):
-    """Time the oracle's per-expert loop, forward + backward, on the first
-    t_slice tokens of the workload (all experts, full width; inputs drawn
-    before the clock starts). Returns (seconds, tokens)."""
+def oracle_sample_time(wl, rows, e):
+    """Time the oracle, as it stands, on a bounded sample of the workload:
+    expert e's forward + backward on its first `rows` routed rows (full H and
+    F, the expert's own weight quantisation included in MXFP8 modes). Inputs
+    are drawn and routed before the clock starts. Returns (seconds, token
+    equivalents = sampled rows / k, rows)."""
     from oracle import moe_oracle as O
-    x, lg, w1, w2, dout = _oracle_inputs(wl, t_slice)
+    d = _oracle_inputs(wl)
+    tok, slot = d["rows"][e]
+    tok, slot = tok[:rows], slot[:rows]
     mx = {"bf16": False, "mxfp8": True, "mxfp8_act4": "act4"}[wl.precision]
+    xe, p, dy = d["x"][tok], d["w"][tok, slot], d["dout"][tok]
     t0 = time.perf_counter()
-    chk = 0.0
-    for e, tok, slot, y2, dxp, dp, dW1e, dW2e in O.layer_fwd_bwd_expert_stream(
-            x, lg, w1, w2, dout, wl.k, mx):
-        chk += float(dW1e[0, 0]) + float(y2.sum())
-    return time.perf_counter() - t0, t_slice
+    y2, saved = O.expert_forward(xe, p, d["w1"][e], d["w2"][e], mx)
+    O.expert_backward(xe, p, d["w1"][e], d["w2"][e], dy, saved, mx)
+    return time.perf_counter() - t0, len(tok) / wl.k, len(tok)
+
+
+def nonempty_experts(wl):
+    return [e for e in range(wl.E) if len(_oracle_inputs(wl)["rows"][e][0]) > 0]
 
 
 def host_cores():
@@ -403,23 +424,26 @@ def max_over_ranks(v, world):
 
 
 def run_reference(args, wl, world, rank):
-    """The oracle, as it stands, on the host cores: a bounded token slice of
-    the workload per step."""
+    """The oracle, as it stands, on the host cores: each step is one expert's
+    forward + backward on its first args.ref_rows routed rows of the workload
+    (the experts taken in turn)."""
     if rank != 0:
         return
     _set_blas_threads()
-    t_slice = args.ref_tokens
-    for _ in range(min(args.warmup, 1)):
-        oracle_sample_time(wl, t_slice)
-    times = []
-    for _ in range(args.steps):
-        dt, n = oracle_sample_time(wl, t_slice)
+    experts = nonempty_experts(wl)
+    for i in range(min(args.warmup, 1)):
+        oracle_sample_time(wl, args.ref_rows, experts[i % len(experts)])
+    times, toks = [], 0.0
+    for i in range(args.steps):
+        dt, n, _ = oracle_sample_time(wl, args.ref_rows, experts[i % len(experts)])
         times.append(dt)
+        toks += n
     tot = sum(times)
-    value = t_slice * args.steps / tot
+    value = toks / tot
     cores = host_cores()
-    sample = (f"first {t_slice} tokens of the {wl.name} workload per step "
-              f"(all {wl.E} experts, full H={wl.H}, F={wl.F}), fwd+bwd, fp64")
+    sample = (f"one expert per step (experts in turn), its first {args.ref_rows} routed rows of "
+              f"the {wl.name} workload (full H={wl.H}, F={wl.F}), fwd+bwd in fp64, counted as "
+              f"rows/k tokens")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -462,37 +486,53 @@ def config_of(wl):
                         f"top-{wl.k} {wl.precision.upper()} fwd+bwd",
             "T": wl.T, "H": wl.H, "F": wl.F, "E": wl.E, "k": wl.k, "precision": wl.precision,
             "global_batch_tokens": wl.T,
-            "l2": "inputs larger than L2 (weights alone 2*E*H*F*3 bytes per step)"}
+            "l2": "inputs larger than L2 (weights alone 2*E*H*F*3 bytes per step)"
+                  if 6 * wl.E * wl.H * wl.F > 126e6 else
+                  "inputs smaller than L2 (latency-bound small case)"}
 
 
-def run_ours(args, wl, world, rank, local):
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
+def is_mx(wl):
+    return wl.precision in ("mxfp8", "mxfp8_act4")
+
+
+def tensor_peak(peaks, mx):
+    """Tensor roofline denominator for the GEMMs' own dtype: the measured BF16
+    burst rate (the timed region is well under a second), times the nominal
+    dense MXFP8/BF16 ratio 4.5/2.25 = 2 for the MXFP8 path."""
+    kind = f"bf16 burst ({peaks['source']})"
+    if mx:
+        return 2.0 * peaks["bf16_tflops"], f"mxfp8 = 2 x {kind}"
+    return peaks["bf16_tflops"], kind
+
+
+def timed_steps(args, wl, world, local, dev):
+    """W untimed steps, then K timed steps of workload wl with CUDA events
+    between the calls on the launching stream. Returns the timing record and
+    the step with its bound tensors."""
     from mixture_experts_expert_sort_b300 import binding as B
-    B.lib()
+    rank = int(os.environ.get("RANK", "0"))
     # Seeded synthetic inputs generated on the device (rank-distinct seeds).
     wlr = wl if rank == 0 else I.Workload(wl.name, wl.T, wl.H, wl.F, wl.E, wl.k, wl.precision,
                                           wl.seed + 100 * rank, wl.zipf_s, wl.zero_experts,
                                           wl.outlier_frac)
     inp = I.make_all(wlr, device=dev)
-    logits, x, w1, w2, dout = inp["logits"], inp["x"], inp["w1"], inp["w2"], inp["dout"]
     T, H, F, E = wl.T, wl.H, wl.F, wl.E
     bf = torch.bfloat16
-    out = torch.empty((T, H), dtype=bf, device=dev)
-    dx = torch.empty((T, H), dtype=bf, device=dev)
-    dw1 = torch.empty((E, H, 2 * F), dtype=bf, device=dev)
-    dw2 = torch.empty((E, F, H), dtype=bf, device=dev)
-    dlogits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    t = {"logits": inp["logits"], "x": inp["x"], "w1": inp["w1"], "w2": inp["w2"],
+         "dout": inp["dout"], "out": torch.empty((T, H), dtype=bf, device=dev),
+         "dx": torch.empty((T, H), dtype=bf, device=dev),
+         "dw1": torch.empty((E, H, 2 * F), dtype=bf, device=dev),
+         "dw2": torch.empty((E, F, H), dtype=bf, device=dev),
+         "dlogits": torch.empty((T, E), dtype=torch.float32, device=dev)}
     step = Step(wl, dev, router=args.router)
-    step.bind(logits, x, w1, w2, dout, out, dx, dw1, dw2, dlogits)
-
+    step.bind(t["logits"], t["x"], t["w1"], t["w2"], t["dout"], t["out"], t["dx"], t["dw1"],
+              t["dw2"], t["dlogits"])
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
     if B.device_error() != 0:
-        raise RuntimeError("device error flag set during warm-up")
+        raise RuntimeError(f"device error flag set during warm-up ({wl.name})")
 
-    # ---- timed region: K steps, per-kernel events on the launching stream
     nk = len(step.NAMES)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
            for _ in range(args.steps)]
@@ -512,28 +552,77 @@ def run_ours(args, wl, world, rank, local):
     clocks.mark_end()
     barrier(world)
     clk = clocks.stop()
-    ms = t0.elapsed_time(t1)
-    ms = max_over_ranks(ms, world)
-    # median over the steps: the first op of the first step also waits for the host
-    per_kernel = {n: statistics.median(evs[i][j].elapsed_time(evs[i][j + 1])
-                                       for i in range(args.steps))
-                  for j, n in enumerate(step.NAMES)}
+    ms = max_over_ranks(t0.elapsed_time(t1), world)
+    # mean over the timed steps, the statistic of ms_per_step
+    per_kernel = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+                  / args.steps for j, n in enumerate(step.NAMES)}
     if B.device_error() != 0:
-        raise RuntimeError("device error flag set during the timed region")
+        raise RuntimeError(f"device error flag set during the timed region ({wl.name})")
+    return {"ms_step": ms / args.steps, "per_kernel": per_kernel, "clocks": clk,
+            "launches": step.launches_per_step * args.steps}, step, t
 
-    # ---- end to end through the public layer API with host buffers
-    # Every step copies its inputs from pinned host memory and reads its
-    # results back, as a training loop does; the copies of one step overlap the
-    # compute of its neighbours (two slots of device buffers, an input-copy
-    # stream and a result-copy stream ordered by events), and the compute stays
-    # on the launching stream. dW stays resident, as in training.
+
+def summarise(wl, rec, world, peaks):
+    """Throughput, GEMM rate and the dominant kernel's roofline of one workload."""
+    ms_step, per_kernel, clk = rec["ms_step"], rec["per_kernel"], rec["clocks"]
+    work = kernel_work(wl)
+    mx = is_mx(wl)
+    gemm_names = [n for n in per_kernel if work[n][0] == "flops"]
+    gemm_ms = sum(per_kernel[n] for n in gemm_names)
+    gemm_tflops = wl.gemm_flops_fwd_bwd() / (gemm_ms / 1000.0) / 1e12
+    peak_t, peak_t_kind = tensor_peak(peaks, mx)
+    dom = max(per_kernel, key=lambda n: per_kernel[n])
+    kind, amount = work[dom]
+    sec = per_kernel[dom] / 1000.0
+    if kind == "flops":
+        ach = amount / sec / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peak_t, "unit": "TFLOP/s",
+                "frac": ach / peak_t, "traffic": None, "kernel": dom, "peak_kind": peak_t_kind,
+                "work_per_launch": amount, "ms_per_launch": per_kernel[dom]}
+    else:
+        ach = amount / sec / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "traffic": None, "kernel": dom,
+                "peak_kind": f"hbm copy ({peaks['source']})", "work_per_launch": amount,
+                "ms_per_launch": per_kernel[dom]}
+    if clk and clk.get("sm_mhz") and kind == "flops":
+        # the same fraction against the burst peak scaled to the sampled SM clock
+        roof["frac_at_sampled_clock"] = roof["frac"] * peaks["sm_max_mhz"] / clk["sm_mhz"]
+    roof["traffic"] = measured_traffic(dom, wl)
+    kern = {}
+    for n in per_kernel:
+        k_, amt = work[n]
+        s = per_kernel[n] / 1000.0
+        kern[n] = {"ms": round(per_kernel[n], 4),
+                   ("tflops" if k_ == "flops" else "gbs"):
+                       round(amt / s / (1e12 if k_ == "flops" else 1e9), 1)}
+    return {
+        "value": world * wl.T / (ms_step / 1000.0), "unit": "tokens/s", "ms_per_step": ms_step,
+        "gemm_tflops": gemm_tflops, "gemm_frac_of_peak": gemm_tflops / peak_t,
+        "gemm_frac_of_spec": gemm_tflops / (4500.0 if mx else 2250.0),
+        "roofline": roof, "clocks": clk, "gpu_launches": rec["launches"], "kernels": kern,
+        "kernels_sum_ms": round(sum(per_kernel.values()), 4),
+    }
+
+
+def e2e_measure(args, step, t, world):
+    """End to end through the public layer API with host buffers. Every step
+    copies its inputs from pinned host memory and reads its results back, as a
+    training loop does; the copies of one step overlap the compute of its
+    neighbours (two slots of device buffers, an input-copy stream and a
+    result-copy stream ordered by events), and the compute stays on the
+    launching stream. dW stays resident, as in training."""
     layer = step.layer
+    x, logits, dout, out, dx, dlogits = t["x"], t["logits"], t["dout"], t["out"], t["dx"], \
+        t["dlogits"]
+    w1, w2, dw1, dw2 = t["w1"], t["w2"], t["dw1"], t["dw2"]
+    T = x.shape[0]
     h_x = x.cpu().pin_memory()
     h_lg = logits.cpu().pin_memory()
     h_do = dout.cpu().pin_memory()
-    h_out = torch.empty((T, H), dtype=bf).pin_memory()
-    h_dx = torch.empty((T, H), dtype=bf).pin_memory()
-    h_dl = torch.empty((T, E), dtype=torch.float32).pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_dx = torch.empty(dx.shape, dtype=dx.dtype).pin_memory()
+    h_dl = torch.empty(dlogits.shape, dtype=dlogits.dtype).pin_memory()
     slots = [{"x": torch.empty_like(x), "lg": torch.empty_like(logits),
               "do": torch.empty_like(dout), "out": torch.empty_like(out),
               "dx": torch.empty_like(dx), "dl": torch.empty_like(dlogits)} for _ in range(2)]
@@ -580,70 +669,73 @@ def run_ours(args, wl, world, rank, local):
     e2e_ms = max_over_ranks(a0.elapsed_time(a1) / e2e_steps, world)
     h2d = h_x.numel() * 2 + h_lg.numel() * 4 + h_do.numel() * 2
     d2h = h_out.numel() * 2 + h_dx.numel() * 2 + h_dl.numel() * 4
+    return {"value": world * T / (e2e_ms / 1000.0), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "api": "moe_layer_forward + moe_layer_backward, host pinned inputs/outputs"}
 
+
+def dtype_of(wl):
+    return ("e4m3 (mxfp8); x, h carried as e2m1 (mxfp4)" if wl.precision == "mxfp8_act4"
+            else "e4m3 (mxfp8)" if is_mx(wl) else "bf16")
+
+
+def run_ours(args, wl, world, rank, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from mixture_experts_expert_sort_b300 import binding as B
+    B.lib()
+    peaks = load_peaks()
+    rec, step, t = timed_steps(args, wl, world, local, dev)
+    e2e = e2e_measure(args, step, t, world)
+    head = summarise(wl, rec, world, peaks)
+    del step, t
+    torch.cuda.empty_cache()
+    # The other workloads, each measured the same way (its own warm-up and K
+    # timed steps), as sub-results of the same line.
+    others = {}
+    names = [] if args.configs == "none" else (
+        [n for n in I.WORKLOADS if n != wl.name] if args.configs == "all"
+        else [n for n in args.configs.split(",") if n and n != wl.name])
+    for n in names:
+        w = I.WORKLOADS[n]
+        r, st, tt = timed_steps(args, w, world, local, dev)
+        s = summarise(w, r, world, peaks)
+        s["config"] = config_of(w)
+        s["dtype"] = dtype_of(w)
+        others[n] = s
+        del st, tt
+        torch.cuda.empty_cache()
     if rank != 0:
         return
-    peaks = load_peaks()
-    ms_step = ms / args.steps
-    tokens_per_s = world * T / (ms_step / 1000.0)
-    work = kernel_work(wl)
-    gemm_names = [n for n, (kind, _) in work.items() if kind == "flops"]
-    gemm_ms = sum(per_kernel[n] for n in gemm_names)
-    gemm_tflops = wl.gemm_flops_fwd_bwd() / (gemm_ms / 1000.0) / 1e12
-    dom = max(per_kernel, key=lambda n: per_kernel[n])
-    kind, amount = work[dom]
-    mx = wl.precision in ("mxfp8", "mxfp8_act4")
-    # Tensor peak for the GEMMs' own dtype: the measured sustained bf16 rate
-    # (kernels timed inside a long step), times the nominal dense MXFP8/BF16
-    # ratio 4.5/2.25 = 2 for the MXFP8 path.
-    tensor_peak = peaks["bf16_tflops_sustained"] * (2.0 if mx else 1.0)
-    tensor_kind = (f"mxfp8 = 2 x bf16 sustained ({peaks['source']})" if mx
-                   else f"bf16 sustained ({peaks['source']})")
-    if kind == "flops":
-        ach = amount / (per_kernel[dom] / 1000.0) / 1e12
-        peak = tensor_peak
-        roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                "frac": ach / peak, "traffic": None, "kernel": dom, "peak_kind": tensor_kind}
-    else:
-        ach = amount / (per_kernel[dom] / 1000.0) / 1e9
-        peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-                "traffic": None, "kernel": dom, "peak_kind": f"hbm copy ({peaks['source']})"}
-    roof["traffic"] = measured_traffic(dom, wl)
-    kern = {}
-    for n in step.NAMES:
-        kind, amount = work[n]
-        t = per_kernel[n] / 1000.0
-        kern[n] = {"ms": round(per_kernel[n], 4),
-                   ("tflops" if kind == "flops" else "gbs"):
-                       round(amount / t / (1e12 if kind == "flops" else 1e9), 1)}
     line = {
-        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("e4m3 (mxfp8); x, h carried as e2m1 (mxfp4)" if wl.precision == "mxfp8_act4"
-                  else "e4m3 (mxfp8)" if mx else "bf16"),
-        "data": "synthetic (seeded, generated on the device)",
+        "dtype": dtype_of(wl), "data": "synthetic (seeded, generated on the device)",
         "config": dict(config_of(wl), router=("router projection x W_r, top-k, aux "
                                               "load-balancing loss and their backward included"
                                               if args.router else "logits given (no router)")),
-        "gemm_tflops": gemm_tflops,
-        "gemm_frac_of_measured_peak": gemm_tflops / tensor_peak,
-        "gemm_frac_of_spec": gemm_tflops / (4500.0 if mx else 2250.0),
-        "roofline": roof,
-        "e2e": {"value": world * T / (e2e_ms / 1000.0), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "api": "moe_layer_forward + moe_layer_backward, host pinned inputs/outputs"},
-        "gpu_launches": step.launches_per_step * args.steps,
-        "clocks": clk,
-        "kernels": kern,
+        "gemm_tflops": head["gemm_tflops"],
+        "gemm_frac_of_peak": head["gemm_frac_of_peak"],
+        "gemm_frac_of_spec": head["gemm_frac_of_spec"],
+        "roofline": head["roofline"],
+        "e2e": e2e,
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
+        "kernels": head["kernels"],
+        "kernels_sum_ms": head["kernels_sum_ms"],
+        "peaks": {k: peaks[k] for k in ("bf16_tflops", "hbm_gbs", "sm_max_mhz", "source")},
+        "workloads": others,
     }
     if world == 1 and not args.no_cpu_baseline:
         _set_blas_threads()
-        dt, n = oracle_sample_time(wl, args.cpu_tokens)
+        e = nonempty_experts(wl)[0]
+        dt, n, rows = oracle_sample_time(wl, args.cpu_rows, e)
         line["cpu_baseline"] = {
             "value": n / dt, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
-            "sample": f"first {n} tokens of the workload, all experts, full width, fwd+bwd, fp64"}
+            "sample": f"expert {e}'s forward+backward on its first {rows} routed rows of the "
+                      f"workload (full H and F), fp64, counted as rows/k = {n:g} tokens; "
+                      f"{dt:.1f} s"}
     print(json.dumps(line), flush=True)
 
 
@@ -718,10 +810,15 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="mixtral", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--workload", default="mixtral_mx", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--configs", default="all",
+                    help="other workloads measured as sub-results of the line: all, none, or "
+                         "a comma-separated list")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=256)
-    ap.add_argument("--ref-tokens", type=int, default=128)
+    ap.add_argument("--cpu-rows", type=int, default=1024,
+                    help="routed rows of one expert in the CPU-baseline sample")
+    ap.add_argument("--ref-rows", type=int, default=128,
+                    help="routed rows of one expert per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling cases)")
     ap.add_argument("--experts", type=int, default=0, help="override E (profiling cases)")
@@ -731,6 +828,7 @@ def main():
     args = ap.parse_args()
     wl = I.WORKLOADS[args.workload]
     if args.tokens or args.experts:
+        args.configs = "none"
         # A reduced case of the same layer shape (H, F, k kept), for profiling.
         wl = I.Workload(wl.name + "_reduced", args.tokens or wl.T, wl.H, wl.F,
                         args.experts or wl.E, wl.k, wl.precision, wl.seed, wl.zipf_s,

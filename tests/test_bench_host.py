@@ -157,7 +157,43 @@ def test_peaks_measured_file_else_fallback(monkeypatch, tmp_path):
     6.4 TB/s, 1.8 PFLOP/s bf16 burst and 1.4 sustained, labelled as such."""
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.load_peaks() == {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0,
-                                  "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+                                  "bf16_tflops_sustained": 1400.0, "sm_max_mhz": 2032.0,
+                                  "source": "fallback"}
     (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 6000.5, "bf16_tflops": 1700.0}')
     assert bench.load_peaks() == {"hbm_gbs": 6000.5, "bf16_tflops": 1700.0,
-                                  "bf16_tflops_sustained": 1700.0, "source": "measured"}
+                                  "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2032.0,
+                                  "source": "measured"}
+
+
+@pytest.mark.parametrize("name", ["mixtral", "mixtral_mx"])
+def test_roofline_fraction_reproduces_from_kernel_time(name):
+    """The line's roofline: the dominant kernel by mean time, achieved = its
+    algorithmic work / its mean time, against the measured BF16 burst peak
+    (x 2, the nominal dense ratio, for MXFP8); the GEMM rate divides the
+    layer's 18 R H F flops by the GEMMs' summed mean times."""
+    wl = I.WORKLOADS[name]
+    work = bench.kernel_work(wl)
+    names = (["route", "plan", "p_rows", "quant_x", "quant_w1", "quant_w2", "fc1_swiglu", "fc2",
+              "unpermute", "quant_dout", "fc2_dgrad_swiglu_bwd", "fc2_wgrad", "fc1_dgrad",
+              "fc1_wgrad", "unpermute_dx", "route_bwd"] if "mx" in name else
+             ["route", "plan", "permute_x", "fc1_swiglu", "fc2", "unpermute", "permute_dout",
+              "fc2_dgrad_swiglu_bwd", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad", "unpermute_dx",
+              "route_bwd"])
+    per = {n: 0.05 for n in names}
+    per.update({"fc1_swiglu": 3.1, "fc1_dgrad": 2.6, "fc1_wgrad": 2.7, "fc2": 1.3,
+                "fc2_dgrad_swiglu_bwd": 2.0, "fc2_wgrad": 1.4})
+    peaks = {"hbm_gbs": 6500.0, "bf16_tflops": 1772.9, "sm_max_mhz": 2032.0,
+             "source": "measured"}
+    rec = {"ms_step": sum(per.values()), "per_kernel": per, "launches": 10,
+           "clocks": {"sm_mhz": 1900.0}}
+    s = bench.summarise(wl, rec, 1, peaks)
+    r = s["roofline"]
+    peak = 1772.9 * (2 if "mx" in name else 1)
+    assert r["kernel"] == "fc1_swiglu" and r["peak"] == peak
+    assert r["achieved"] == pytest.approx(work["fc1_swiglu"][1] / 3.1e-3 / 1e12)
+    assert r["frac"] == pytest.approx(r["achieved"] / peak)
+    assert r["frac_at_sampled_clock"] == pytest.approx(r["frac"] * 2032.0 / 1900.0)
+    gemm_ms = 3.1 + 2.6 + 2.7 + 1.3 + 2.0 + 1.4
+    assert s["gemm_tflops"] == pytest.approx(18.0 * wl.R * wl.H * wl.F / gemm_ms / 1e9)
+    assert s["kernels_sum_ms"] == pytest.approx(sum(per.values()), abs=1e-3)
+    assert s["value"] == pytest.approx(wl.T / (rec["ms_step"] / 1000.0))
