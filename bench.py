@@ -36,6 +36,7 @@ import sys
 import tempfile
 import time
 
+import numpy as np
 import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -357,22 +358,29 @@ def _oracle_inputs(wl):
     return _ORACLE_INPUTS[wl.name]
 
 
-def oracle_sample_time(wl, rows, e):
+def oracle_sample_time(wl, rows, e, ffn=None):
     """Time the oracle, as it stands, on a bounded sample of the workload:
-    expert e's forward + backward on its first `rows` routed rows (full H and
-    F, the expert's own weight quantisation included in MXFP8 modes). Inputs
-    are drawn and routed before the clock starts. Returns (seconds, token
-    equivalents = sampled rows / k, rows)."""
+    expert e's forward + backward on its first `rows` routed rows, full H,
+    and the first `ffn` FFN columns (all F when None; the expert MLP is a sum
+    over FFN columns, so a column slice is the same computation on a
+    narrower expert; a slice of whole 32-blocks keeps every MXFP8 block
+    whole). The sample's share of the expert's weight quantisation is
+    included in MXFP8 modes. Inputs are drawn and routed before the clock
+    starts. Returns (seconds, token equivalents = rows / k * ffn / F, rows,
+    ffn)."""
     from oracle import moe_oracle as O
     d = _oracle_inputs(wl)
     tok, slot = d["rows"][e]
     tok, slot = tok[:rows], slot[:rows]
     mx = {"bf16": False, "mxfp8": True, "mxfp8_act4": "act4"}[wl.precision]
+    fs = wl.F if ffn is None else min(ffn, wl.F)
+    cols = np.concatenate([np.arange(fs), wl.F + np.arange(fs)])
+    w1e, w2e = d["w1"][e][:, cols], d["w2"][e][:fs]
     xe, p, dy = d["x"][tok], d["w"][tok, slot], d["dout"][tok]
     t0 = time.perf_counter()
-    y2, saved = O.expert_forward(xe, p, d["w1"][e], d["w2"][e], mx)
-    O.expert_backward(xe, p, d["w1"][e], d["w2"][e], dy, saved, mx)
-    return time.perf_counter() - t0, len(tok) / wl.k, len(tok)
+    y2, saved = O.expert_forward(xe, p, w1e, w2e, mx)
+    O.expert_backward(xe, p, w1e, w2e, dy, saved, mx)
+    return time.perf_counter() - t0, len(tok) / wl.k * fs / wl.F, len(tok), fs
 
 
 def nonempty_experts(wl):
@@ -432,18 +440,19 @@ def run_reference(args, wl, world, rank):
     _set_blas_threads()
     experts = nonempty_experts(wl)
     for i in range(min(args.warmup, 1)):
-        oracle_sample_time(wl, args.ref_rows, experts[i % len(experts)])
+        oracle_sample_time(wl, args.ref_rows, experts[i % len(experts)], args.ref_ffn)
     times, toks = [], 0.0
     for i in range(args.steps):
-        dt, n, _ = oracle_sample_time(wl, args.ref_rows, experts[i % len(experts)])
+        dt, n, _, fs = oracle_sample_time(wl, args.ref_rows, experts[i % len(experts)],
+                                          args.ref_ffn)
         times.append(dt)
         toks += n
     tot = sum(times)
     value = toks / tot
     cores = host_cores()
-    sample = (f"one expert per step (experts in turn), its first {args.ref_rows} routed rows of "
-              f"the {wl.name} workload (full H={wl.H}, F={wl.F}), fwd+bwd in fp64, counted as "
-              f"rows/k tokens")
+    sample = (f"one expert per step (experts in turn): its first {args.ref_rows} routed rows of "
+              f"the {wl.name} workload, full H={wl.H}, the first {fs} of F={wl.F} FFN columns, "
+              f"fwd+bwd in fp64, counted as rows/k * {fs}/{wl.F} tokens")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -730,7 +739,7 @@ def run_ours(args, wl, world, rank, local):
     if world == 1 and not args.no_cpu_baseline:
         _set_blas_threads()
         e = nonempty_experts(wl)[0]
-        dt, n, rows = oracle_sample_time(wl, args.cpu_rows, e)
+        dt, n, rows, _ = oracle_sample_time(wl, args.cpu_rows, e)
         line["cpu_baseline"] = {
             "value": n / dt, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
             "sample": f"expert {e}'s forward+backward on its first {rows} routed rows of the "
@@ -815,10 +824,12 @@ def main():
                     help="other workloads measured as sub-results of the line: all, none, or "
                          "a comma-separated list")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-rows", type=int, default=1024,
+    ap.add_argument("--cpu-rows", type=int, default=2048,
                     help="routed rows of one expert in the CPU-baseline sample")
-    ap.add_argument("--ref-rows", type=int, default=128,
+    ap.add_argument("--ref-rows", type=int, default=512,
                     help="routed rows of one expert per step of the reference arm")
+    ap.add_argument("--ref-ffn", type=int, default=1024,
+                    help="FFN columns of that expert per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling cases)")
     ap.add_argument("--experts", type=int, default=0, help="override E (profiling cases)")
