@@ -30,10 +30,9 @@
 // Every wait is bounded: after kWaitLimitNs the kernel records
 // MOE_DEVERR_TIMEOUT, stops issuing work, lets its copies land, frees TMEM
 // and returns.
-#include <cudaTypedefs.h>
-
 #include "common.cuh"
 #include "ptx.cuh"
+#include "tmap.cuh"
 
 namespace moe {
 namespace gemm {
@@ -502,35 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* ptr = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// 2-D row-major tensor [rows, cols] of `elem_bytes` elements, box [box_rows, box_cols],
-// 128-byte swizzle (box_cols * elem_bytes must be <= 128).
-static bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes,
-                      long long rows, long long cols, long long ld, int box_rows, int box_cols,
-                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(ld * elem_bytes)};
-  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
+using moe::make_tmap;
 
 // K-major BF16 operands: 128-byte rows, 128-byte swizzle (matches kSwizzle128B).
 constexpr CUtensorMapSwizzle kKSwz = CU_TENSOR_MAP_SWIZZLE_128B;

@@ -26,7 +26,15 @@
 //    Row-wise blocks (32 columns of one row) are quantised by their lane.
 //    Column-wise blocks (one column over the warp's 32 rows) are transposed
 //    through a per-warp shared-memory buffer, after which each lane holds one
-//    column and quantises it like a row, storing its 32 contiguous bytes.
+//    column and quantises it like a row.
+//  * Epilogue memory traffic goes through TMA. A warp-wide store or load in
+//    which every lane touches a different row costs the L1 one pass per
+//    cache line (32 per instruction), which starved these epilogues. So the
+//    code bytes of every 32 x 32 block are staged in the warp's buffer and
+//    written by TMA tensor stores, and the backward reads the saved gate/up
+//    values through TMA loads (one mbarrier per epilogue warp, prefetched a
+//    chunk ahead). Only the scale bytes (four cache lines per warp store)
+//    are stored directly.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -55,7 +63,15 @@ constexpr int kTxBytes = kStageBytes + kSfStageBytes;
 // (rows 16-byte aligned for vector writes; column reads hit 32 banks).
 constexpr int kXposeStride = 36;
 constexpr int kXposeWords = 32 * kXposeStride;
-constexpr int kGuRowBytes = 144;
+// Per-warp buffer: the transposes use its first 4608 bytes; afterwards it
+// stages the warp's 32 x 32-byte code boxes (1 KB each, 32-byte swizzle) for
+// TMA stores. 1024-byte aligned so that every box is swizzle-aligned.
+constexpr int kWarpBufBytes = 5120;
+// Per-warp gate/up staging: two 32 x 32 bf16 boxes (64-byte rows, 64-byte
+// swizzle): the backward's TMA loads, the forward's TMA stores.
+constexpr int kGuBytes = 4096;
+
+__host__ __device__ constexpr int round1024(int x) { return (x + 1023) / 1024 * 1024; }
 
 // Shared-memory layout and warp counts of one kernel flavour. The plain
 // (store / wgrad) kernels use a 4-stage ring and 4 epilogue warps; the fused
@@ -71,15 +87,11 @@ struct Cfg {
   // A/B stages stay 1024-byte aligned (128B-swizzle atoms); the scale tiles
   // of all stages follow in a region of their own.
   static constexpr int kSfOffset = kStages * kStageBytes;
-  static constexpr int kXposeOffset = kSfOffset + kStages * kSfStageBytes;
-  // Per-warp staging of gate/up: the backward epilogue reads the saved values
-  // through it (cp.async; 32 rows x (64 B gate + 64 B up), rows padded to
-  // 144 B); the forward epilogue writes its gate and up boxes (2 x 2 KB)
-  // there for TMA stores. 128-byte aligned.
-  static constexpr int kGuOffset = kXposeOffset + (FUSED ? kEpiWarps * kXposeWords * 4 : 0);
-  static constexpr int kBarOffset = kGuOffset + (FUSED ? kEpiWarps * 32 * kGuRowBytes : 0);
-  // full[S], empty[S], tfull[2], region_empty[3], drain
-  static constexpr int kNumBars = 2 * kStages + 6;
+  static constexpr int kXposeOffset = round1024(kSfOffset + kStages * kSfStageBytes);
+  static constexpr int kGuOffset = kXposeOffset + (FUSED ? kEpiWarps * kWarpBufBytes : 0);
+  static constexpr int kBarOffset = kGuOffset + (FUSED ? kEpiWarps * kGuBytes : 0);
+  // full[S], empty[S], tfull[2], region_empty[3], drain, gate/up loads[epilogue warps]
+  static constexpr int kNumBars = 2 * kStages + 6 + (FUSED ? kEpiWarps : 0);
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
   static constexpr int kPrefixOffset = kMiscOffset + 16;
   static constexpr int kSmemBytes = kPrefixOffset + (kMaxGroups + 1) * 4;
@@ -161,15 +173,14 @@ __device__ __forceinline__ int b_half_row(const MxParams& p, int nt, int h) {
 
 // ---------------------------------------------------------------- epilogue helpers
 
-// Row-wise MXFP8 of 32 consecutive values held by one thread: 32 code bytes
-// to dst (16-byte aligned) and the scale byte to *sdst.
-__device__ __forceinline__ void quant_row32(const float* v, uint8_t* dst, uint8_t* sdst) {
+// MXFP8 of 32 consecutive values held by one thread: their 32 E4M3 codes in
+// w[0..7] (value 4i + j in byte j of w[i]); returns the E8M0 scale byte.
+__device__ __forceinline__ uint32_t quant32(const float* v, uint32_t* w) {
   // Non-negative floats order like their bit patterns; Inf and NaN are the largest.
   uint32_t mbits = 0;
 #pragma unroll
   for (int i = 0; i < 32; ++i) mbits = max(mbits, __float_as_uint(v[i]) & 0x7FFFFFFFu);
   const uint32_t sb = mbits < 0x7F800000u ? mx_scale_byte(__uint_as_float(mbits)) : 0xFFu;
-  uint32_t w[8];
   if (sb == 0xFFu) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = 0x7F7F7F7Fu;
@@ -180,21 +191,17 @@ __device__ __forceinline__ void quant_row32(const float* v, uint8_t* dst, uint8_
       w[i] = (uint32_t)cvt_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) |
              ((uint32_t)cvt_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
   }
-  uint4* o = reinterpret_cast<uint4*>(dst);
-  o[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  o[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  *sdst = (uint8_t)sb;
+  return sb;
 }
 
 // Column-wise MXFP8 of a 32 x 32 block held one row per lane (v[i] is row
 // `lane`, column i): every column is one block. The block is transposed
 // through this warp's buffer `xs` (32 rows of kXposeStride words), after
-// which lane c holds column c and quantises it like a row: its 32 codes go to
-// q + (f0 + c) * ld + rb and its scale byte to the tiled layout of an operand
-// with ld columns. Called by all 32 lanes of the warp.
-__device__ __forceinline__ void quant_col_block32(const float* v, uint8_t* q, uint8_t* sq,
-                                                  long long ld, long long f0, long long rb,
-                                                  float* xs, int lane) {
+// which lane c holds column c and quantises it: its 32 codes go to w[0..7]
+// and its scale byte to the tiled layout of an operand with ld columns (row
+// f0 + c, 32-row block rb / 32). Called by all 32 lanes.
+__device__ __forceinline__ void quant_col32(const float* v, uint32_t* w, uint8_t* sq, long long ld,
+                                            long long f0, long long rb, float* xs, int lane) {
   __syncwarp();
   float4* row = reinterpret_cast<float4*>(xs + lane * kXposeStride);
 #pragma unroll
@@ -203,7 +210,18 @@ __device__ __forceinline__ void quant_col_block32(const float* v, uint8_t* q, ui
   float c[32];
 #pragma unroll
   for (int r = 0; r < 32; ++r) c[r] = xs[r * kXposeStride + lane];
-  quant_row32(c, q + (f0 + lane) * ld + rb, sq + mx_scale_offset(f0 + lane, rb >> 5, ld));
+  sq[mx_scale_offset(f0 + lane, rb >> 5, ld)] = (uint8_t)quant32(c, w);
+}
+
+// Lane `lane`'s 32 code bytes into row `lane` of a 32 x 32-byte box at `box`
+// (1 KB, 256-byte aligned), in the 32-byte swizzle a TMA store with
+// CU_TENSOR_MAP_SWIZZLE_32B reads: 16-byte chunk i of row r sits at chunk
+// i ^ ((r >> 2) & 1). Row r and r + 4 then fall in different bank halves.
+__device__ __forceinline__ void stage_codes(uint8_t* box, int lane, const uint32_t* w) {
+  uint4* d = reinterpret_cast<uint4*>(box + lane * 32);
+  const int sw = (lane >> 2) & 1;
+  d[sw] = make_uint4(w[0], w[1], w[2], w[3]);
+  d[sw ^ 1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 // Tile-local accumulator chunk c (32 columns) of this warp's 32 rows: from
@@ -231,18 +249,30 @@ __device__ __forceinline__ void acc_chunk(int c, bool odd, int h, const float* s
   }
 }
 
-// Asynchronous copy of this lane's row of a 32-column gate/up chunk
-// (2 x 64 bytes of bf16) into its staging row in shared memory.
-__device__ __forceinline__ void stage_gu_chunk(const MxParams& p, long long grow, long long col,
-                                               uint32_t dst) {
-  const __nv_bfloat16* g = p.GU + grow * 2 * p.F + col;
-  const __nv_bfloat16* u = g + p.F;
+// TMA load of the gate and up boxes (32 rows x 32 columns of bf16, 64-byte
+// swizzle) of gate/up column `col` and row `rb` into this warp's staging
+// buffer, completing on `bar`. Issued by one lane.
+__device__ __forceinline__ void load_gu(const CUtensorMap* tm_gu, uint32_t dst, int col, int F,
+                                        int rb, uint32_t bar) {
+  ptx::mbar_arrive_expect_tx(bar, kGuBytes);
+  ptx::tma_load_2d(dst, tm_gu, col, rb, bar);
+  ptx::tma_load_2d(dst + 2048, tm_gu, F + col, rb, bar);
+}
+
+// Accumulator chunk c (tile-local, 32 columns) of this warp's 32 rows: a copy
+// of `regs` when given (the chunk drained from the shared TMEM region), else
+// read from TMEM.
+__device__ __forceinline__ void load_acc(int c, const float* regs, uint32_t tl_tile, float* f) {
+  if (regs) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    ptx::cp_async_16(dst + 16 * i, g + 8 * i);
-    ptx::cp_async_16(dst + 64 + 16 * i, u + 8 * i);
+    for (int i = 0; i < 32; ++i) f[i] = regs[i];
+  } else {
+    uint32_t v[32];
+    ptx::tmem_ld_32x32b_x32(tl_tile + c * 32, v);
+    ptx::tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
   }
-  ptx::cp_async_commit();
 }
 
 // Element i (a compile-time index after unrolling) of 32 packed bf16 values.
@@ -265,6 +295,160 @@ __device__ __forceinline__ void unpack_bf16x32(const uint4* s, float* v) {
   }
 }
 
+// FC1 + SwiGLU epilogue of one gate/up chunk pair c (h-columns
+// nt*128 + c*32 + [0, 32)) for this warp's 32 rows: [g | u] to bf16 through
+// TMA stores, then H = silu(g) u p quantised row- and column-wise, its code
+// boxes written by TMA. g_regs / u_regs: the drained shared-region chunk, if
+// this pair holds it.
+__device__ __forceinline__ void fwd_pair(const MxParams& p, const TileInfo& ti, int c,
+                                         const float* g_regs, const float* u_regs, float pr,
+                                         bool row_ok, long long grow, long long rb,
+                                         uint32_t tl_tile, int lane, float* xs,
+                                         uint8_t* gu_stage, const CUtensorMap* tm_gu,
+                                         const CUtensorMap* tm_qr, const CUtensorMap* tm_qc) {
+  const long long F = p.F;
+  uint8_t* xb = reinterpret_cast<uint8_t*>(xs);
+  float g[32], u[32];
+  load_acc(c, g_regs, tl_tile, g);
+  load_acc(c + 4, u_regs, tl_tile, u);
+  const long long col = (long long)ti.nt * (BN / 2) + c * 32;
+  // [g | u] in bf16: the warp's 32 x 32 gate and up boxes are staged in shared
+  // memory (row `lane` = 64 bytes each) and written by TMA. The wait also
+  // frees this warp's code boxes of its previous chunk.
+  if (lane == 0) ptx::bulk_wait_read_all();
+  __syncwarp();
+  gemm::store32_bf16(reinterpret_cast<__nv_bfloat16*>(gu_stage + lane * 64), g);
+  gemm::store32_bf16(reinterpret_cast<__nv_bfloat16*>(gu_stage + 2048 + lane * 64), u);
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    const uint32_t sa = ptx::smem_u32(gu_stage);
+    ptx::tma_store_2d(tm_gu, (int)col, (int)rb, sa);
+    ptx::tma_store_2d(tm_gu, (int)(F + col), (int)rb, sa + 2048);
+    ptx::bulk_commit_group();
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) g[i] = g[i] * gemm::sigmoidf_fast(g[i]) * u[i] * pr;  // h
+  // H: the column-wise block through the transpose, then the row-wise block.
+  uint32_t wc[8], wr[8];
+  quant_col32(g, wc, p.s_col, p.q_col_ld, col, rb, xs, lane);
+  const uint32_t sb = quant32(g, wr);
+  if (row_ok) p.s_row[mx_scale_offset(grow, col >> 5, p.q_row_ld)] = (uint8_t)sb;
+  __syncwarp();  // every lane has read its column out of the buffer
+  stage_codes(xb, lane, wr);
+  stage_codes(xb + 1024, lane, wc);
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    const uint32_t xb_s = ptx::smem_u32(xb);
+    ptx::tma_store_2d(tm_qr, (int)col, (int)rb, xb_s);
+    ptx::tma_store_2d(tm_qc, (int)rb, (int)col, xb_s + 1024);
+    ptx::bulk_commit_group();
+  }
+}
+
+// The FC2-dgrad epilogue's chunks for a warp of parity h: tile-local chunks
+// h, h + 2, h + 4, h + 6 that lie inside the tile's ncol columns, the one in
+// the shared TMEM region (h of odd tiles, 6 + h of even ones) first. Four
+// bits per chunk in bits 0..15, the count in bits 16 and up.
+__host__ __device__ __forceinline__ uint32_t bwd_chunk_order(bool odd, int h, int ncol) {
+  const int cs = odd ? h : 6 + h;
+  uint32_t ord = 0;
+  int n = 0;
+  if (cs * 32 < ncol) ord |= (uint32_t)cs << (4 * n++);
+  for (int c = h; c < 8; c += 2)
+    if (c != cs && c * 32 < ncol) ord |= (uint32_t)c << (4 * n++);
+  return ord | ((uint32_t)n << 16);
+}
+
+// Column block of gate/up chunk c (tile-local) of tile ti.
+__device__ __forceinline__ int bwd_col(const TileInfo& ti, int c) { return ti.nt * BN + c * 32; }
+
+// FC2-dgrad + SwiGLU-backward epilogue of the i-th chunk of `ord` for this
+// warp's 32 rows. dH comes from `regs` (the drained shared-region chunk) or
+// TMEM; the saved gate/up from this warp's TMA boxes (waited on here; the
+// next chunk's boxes are requested as soon as these are read); dY1 = [dg | du]
+// is quantised row- and column-wise and its four code boxes written by TMA;
+// this chunk's part of dL/dp is added to dp. Returns false on an abort.
+__device__ __forceinline__ bool bwd_chunk(const MxParams& p, const TileInfo& ti, uint32_t ord,
+                                          int i, const float* regs, float pr, bool row_ok,
+                                          long long grow, long long rb, uint32_t tl_tile,
+                                          int lane, float* xs, uint8_t* gu_stage,
+                                          const CUtensorMap* tm_gu, const CUtensorMap* tm_qr,
+                                          const CUtensorMap* tm_qc, uint32_t gu_bar,
+                                          uint32_t& gu_phase, bool& gu_pending,
+                                          volatile int* s_abort, float& dp) {
+  const long long F = p.F;
+  const int n = (int)(ord >> 16);
+  const int c = (int)((ord >> (4 * i)) & 15);
+  const long long col = bwd_col(ti, c);
+  uint8_t* xb = reinterpret_cast<uint8_t*>(xs);
+  float dg[32], du[32];
+  load_acc(c, regs, tl_tile, dg);  // dH for now
+  if (!gemm::wait_bar(gu_bar, gu_phase, s_abort)) return false;
+  gu_phase ^= 1u;
+  gu_pending = false;
+  // Lane r reads row r of the boxes, whose 16-byte chunk j sits at
+  // j ^ ((r >> 1) & 3) under the 64-byte swizzle.
+  const int sw = (lane >> 1) & 3;
+  const uint4* g_row = reinterpret_cast<const uint4*>(gu_stage + lane * 64);
+  const uint4* u_row = reinterpret_cast<const uint4*>(gu_stage + 2048 + lane * 64);
+  uint4 gc[4], uc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    gc[j] = g_row[j ^ sw];
+    uc[j] = u_row[j ^ sw];
+  }
+  __syncwarp();  // the warp is done reading the boxes
+  if (i + 1 < n) {
+    if (lane == 0) {
+      ptx::fence_proxy_async_smem();
+      load_gu(tm_gu, ptx::smem_u32(gu_stage), bwd_col(ti, (int)((ord >> (4 * (i + 1))) & 15)),
+              (int)F, (int)rb, gu_bar);
+    }
+    gu_pending = true;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float g = bf16_at(gc, j), u = bf16_at(uc, j);
+    const float sg = gemm::sigmoidf_fast(g);
+    const float silu = g * sg;
+    dp = fmaf(dg[j], silu * u, dp);
+    const float da = dg[j] * pr;  // dA = dH * p
+    dg[j] = da * u * sg * (1.f + g * (1.f - sg));
+    du[j] = da * silu;
+  }
+  // dg into columns [0, F), du into [F, 2F), both directions: the column-wise
+  // blocks through the transpose, then the row-wise ones; the four code boxes
+  // go out by TMA.
+  if (lane == 0) ptx::bulk_wait_read_all();  // the previous chunk's boxes were read
+  __syncwarp();
+  uint32_t cg[8], cu[8], rg[8], ru[8];
+  quant_col32(dg, cg, p.s_col, p.q_col_ld, col, rb, xs, lane);
+  quant_col32(du, cu, p.s_col, p.q_col_ld, F + col, rb, xs, lane);
+  const uint32_t sbg = quant32(dg, rg), sbu = quant32(du, ru);
+  if (row_ok) {
+    p.s_row[mx_scale_offset(grow, col >> 5, p.q_row_ld)] = (uint8_t)sbg;
+    p.s_row[mx_scale_offset(grow, (F + col) >> 5, p.q_row_ld)] = (uint8_t)sbu;
+  }
+  __syncwarp();  // every lane has read its column out of the buffer
+  stage_codes(xb, lane, rg);
+  stage_codes(xb + 1024, lane, ru);
+  stage_codes(xb + 2048, lane, cg);
+  stage_codes(xb + 3072, lane, cu);
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    const uint32_t xb_s = ptx::smem_u32(xb);
+    ptx::tma_store_2d(tm_qr, (int)col, (int)rb, xb_s);
+    ptx::tma_store_2d(tm_qr, (int)(F + col), (int)rb, xb_s + 1024);
+    ptx::tma_store_2d(tm_qc, (int)rb, (int)col, xb_s + 2048);
+    ptx::tma_store_2d(tm_qc, (int)rb, (int)(F + col), xb_s + 3072);
+    ptx::bulk_commit_group();
+  }
+  return true;
+}
+
 // The epilogue of one tile for this warp's 32 rows (lane = row). Fused
 // epilogues split the tile's 32-column chunks between two warps per lane
 // quarter by parity h; the plain ones take every chunk (h = 0, NSH = 2).
@@ -272,7 +456,10 @@ template <int MODE, int EPI>
 __device__ __forceinline__ void epilogue_tile(const MxParams& p, const TileInfo& ti, bool odd,
                                               int h, const float* sh, uint32_t tl_tile, int q,
                                               int lane, float* xs, uint8_t* gu_stage,
-                                              const CUtensorMap* tm_gu) {
+                                              const CUtensorMap* tm_gu, const CUtensorMap* tm_qr,
+                                              const CUtensorMap* tm_qc, uint32_t gu_bar,
+                                              uint32_t& gu_phase, bool& gu_pending,
+                                              volatile int* s_abort) {
   const long long lrow = (long long)ti.mt * BM + q * 32 + lane;
   const bool has_acc = ti.k_iters > 0;
   if (MODE == WGRAD) {
@@ -305,80 +492,34 @@ __device__ __forceinline__ void epilogue_tile(const MxParams& p, const TileInfo&
     }
   } else if (EPI == EPI_SWIGLU_FWD) {
     // Tile-local chunks 0..3 are gate, 4..7 are up, for F-columns n0 .. n0+127;
-    // this warp takes h-columns chunks c = h, h + 2.
+    // this warp takes the h-column chunks c = h, h + 2. The pair holding its
+    // drained shared-region chunk (local chunk h of odd tiles, 6 + h of even
+    // ones) goes first, outside the loop, so those registers are free after it.
     const float pr = row_ok ? p.p_rows[grow] : 0.f;
-    const long long F = p.F;
-#pragma unroll 1
-    for (int c = h; c < 4; c += 2) {
-      float g[32], u[32];
-      acc_chunk<1>(c, odd, h, sh, tl_tile, g);
-      acc_chunk<1>(c + 4, odd, h, sh, tl_tile, u);
-      const long long col = (long long)ti.nt * (BN / 2) + c * 32;
-      // [g | u] in bf16: the warp's 32 x 32 gate and up boxes are staged in
-      // shared memory (row `lane` = 64 bytes each) and written by TMA.
-      if (lane == 0) ptx::bulk_wait_read_all();  // previous boxes have been read
-      __syncwarp();
-      gemm::store32_bf16(reinterpret_cast<__nv_bfloat16*>(gu_stage + lane * 64), g);
-      gemm::store32_bf16(reinterpret_cast<__nv_bfloat16*>(gu_stage + 2048 + lane * 64), u);
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        const uint32_t sa = ptx::smem_u32(gu_stage);
-        ptx::tma_store_2d(tm_gu, (int)col, (int)rb, sa);
-        ptx::tma_store_2d(tm_gu, (int)(F + col), (int)rb, sa + 2048);
-        ptx::bulk_commit_group();
-      }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) g[i] = g[i] * gemm::sigmoidf_fast(g[i]) * u[i] * pr;  // h
-      if (row_ok)
-        quant_row32(g, p.q_row + grow * p.q_row_ld + col,
-                    p.s_row + mx_scale_offset(grow, col >> 5, p.q_row_ld));
-      quant_col_block32(g, p.q_col, p.s_col, p.q_col_ld, col, rb, xs, lane);
-    }
+    const int c0 = odd ? h : 2 + h;
+    fwd_pair(p, ti, c0, odd ? sh : nullptr, odd ? nullptr : sh, pr, row_ok, grow, rb, tl_tile,
+             lane, xs, gu_stage, tm_gu, tm_qr, tm_qc);
+    fwd_pair(p, ti, c0 ^ 2, nullptr, nullptr, pr, row_ok, grow, rb, tl_tile, lane, xs, gu_stage,
+             tm_gu, tm_qr, tm_qc);
   } else {  // EPI_SWIGLU_BWD: accumulator = dH for F-columns nt*256 + [0, 256)
     const float pr = row_ok ? p.p_rows[grow] : 0.f;
-    const long long F = p.F;
     const int ncol = p.N - ti.nt * BN;
     float dp = 0.f;
-    // Saved gate/up of this warp's next chunk, staged into shared memory
-    // while the current chunk is quantised (rows are whole 128-row groups,
-    // so every lane's row is valid).
-    const uint32_t gu_row = ptx::smem_u32(gu_stage) + lane * kGuRowBytes;
-    const uint4* gu_mine = reinterpret_cast<const uint4*>(gu_stage + lane * kGuRowBytes);
-    if (h * 32 < ncol) stage_gu_chunk(p, grow, (long long)ti.nt * BN + h * 32, gu_row);
+    // This warp's chunks (parity h, inside the N tail), four bits each, the
+    // one in the shared TMEM region first: it is processed from the drained
+    // registers outside the loop, which frees them for the rest.
+    const uint32_t ord = bwd_chunk_order(odd, h, ncol);
+    const int n = (int)(ord >> 16);
+    const bool first_shared = n > 0 && (int)(ord & 15) == (odd ? h : 6 + h);
+    if (n > 0 && !bwd_chunk(p, ti, ord, 0, first_shared ? sh : nullptr, pr, row_ok, grow, rb,
+                            tl_tile, lane, xs, gu_stage, tm_gu, tm_qr, tm_qc, gu_bar, gu_phase,
+                            gu_pending, s_abort, dp))
+      return;
 #pragma unroll 1
-    for (int c = h; c < 8 && c * 32 < ncol; c += 2) {  // N tail: uniform across the warp
-      const long long col = (long long)ti.nt * BN + c * 32;
-      float dg[32], du[32];
-      acc_chunk<1>(c, odd, h, sh, tl_tile, dg);  // dH for now
-      ptx::cp_async_wait_all();
-      uint4 gc[4], uc[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        gc[i] = gu_mine[i];
-        uc[i] = gu_mine[4 + i];
-      }
-      if (c + 2 < 8 && (c + 2) * 32 < ncol) stage_gu_chunk(p, grow, col + 64, gu_row);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float g = bf16_at(gc, i), u = bf16_at(uc, i);
-        const float sg = gemm::sigmoidf_fast(g);
-        const float silu = g * sg;
-        dp = fmaf(dg[i], silu * u, dp);
-        const float da = dg[i] * pr;  // dA = dH * p
-        dg[i] = da * u * sg * (1.f + g * (1.f - sg));
-        du[i] = da * silu;
-      }
-      // dg into columns [0, F), du into [F, 2F), both directions.
-      if (row_ok) {
-        quant_row32(dg, p.q_row + grow * p.q_row_ld + col,
-                    p.s_row + mx_scale_offset(grow, col >> 5, p.q_row_ld));
-        quant_row32(du, p.q_row + grow * p.q_row_ld + F + col,
-                    p.s_row + mx_scale_offset(grow, (F + col) >> 5, p.q_row_ld));
-      }
-      quant_col_block32(dg, p.q_col, p.s_col, p.q_col_ld, col, rb, xs, lane);
-      quant_col_block32(du, p.q_col, p.s_col, p.q_col_ld, F + col, rb, xs, lane);
-    }
+    for (int i = 1; i < n; ++i)
+      if (!bwd_chunk(p, ti, ord, i, nullptr, pr, row_ok, grow, rb, tl_tile, lane, xs, gu_stage,
+                     tm_gu, tm_qr, tm_qc, gu_bar, gu_phase, gu_pending, s_abort, dp))
+        return;
     // This warp's partial of dL/dp over its chunks; the two warps of a lane
     // quarter write the two halves of the tile's partial (n_part = 2 per tile).
     if (row_ok) p.dp_part[grow * p.n_part + 2 * ti.nt + h] = dp;
@@ -389,7 +530,9 @@ template <int MODE, int EPI>
 __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
     grouped_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
-                             const __grid_constant__ CUtensorMap tmC, const MxParams p) {
+                             const __grid_constant__ CUtensorMap tmC,
+                             const __grid_constant__ CUtensorMap tmQr,
+                             const __grid_constant__ CUtensorMap tmQc, const MxParams p) {
   using L = Cfg<EPI != EPI_STORE>;
   constexpr int kStages = L::kStages;
   constexpr int kSfOffset = L::kSfOffset;
@@ -409,6 +552,8 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
   // 2 = [256, 448) (odd tiles only).
   auto region_bar = [&](int r) { return bar0 + 8u * (2 * kStages + 2 + r); };
   const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 5);
+  // gate/up loads of epilogue warp w (fused kernels)
+  auto gu_bar_of = [&](int w) { return bar0 + 8u * (2 * kStages + 6 + w); };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kMiscOffset);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kMiscOffset + 4);
   int* s_prefix = reinterpret_cast<int*>(smem + kPrefixOffset);
@@ -424,6 +569,8 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
     for (int b = 0; b < 2; ++b) ptx::mbar_init(tfull_bar(b), 1);
     for (int r = 0; r < 3; ++r) ptx::mbar_init(region_bar(r), kEpiThreads);
     ptx::mbar_init(drain_bar, 1);
+    if (EPI != EPI_STORE)
+      for (int w = 0; w < L::kEpiWarps; ++w) ptx::mbar_init(gu_bar_of(w), 1);
     ptx::fence_mbar_init();
     *s_abort = 0;
     int acc = 0;
@@ -445,6 +592,11 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
+    if (EPI != EPI_STORE) {
+      ptx::tma_prefetch_desc(&tmC);
+      ptx::tma_prefetch_desc(&tmQr);
+      ptx::tma_prefetch_desc(&tmQc);
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(s_tmem), 512);
@@ -581,14 +733,30 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
     const int q = warp & 3;          // TMEM lane quarter this warp may access
     const int h = (warp - 2) >> 2;   // chunk parity (fused: two warps per quarter)
     constexpr int NSH = L::kEpiWarps == 8 ? 1 : 2;  // shared chunks drained per warp
-    float* xs = reinterpret_cast<float*>(smem + L::kXposeOffset) + (warp - 2) * kXposeWords;
-    uint8_t* gu_stage = smem + L::kGuOffset + (warp - 2) * 32 * kGuRowBytes;
+    float* xs = reinterpret_cast<float*>(smem + L::kXposeOffset + (warp - 2) * kWarpBufBytes);
+    uint8_t* gu_stage = smem + L::kGuOffset + (warp - 2) * kGuBytes;
+    const uint32_t gu_bar = gu_bar_of(warp - 2);
+    uint32_t gu_phase = 0;
+    bool gu_pending = false;  // a gate/up load of this warp is in flight
     const uint32_t tl_lanes = tmem_base + ((uint32_t)(q * 32) << 16);
     int e_hint = 0;
     int j = 0;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++j) {
       TileInfo ti;
       decode_tile<MODE>(p, s_prefix, t, e_hint, ti);
+      if (EPI == EPI_SWIGLU_BWD) {
+        // The saved gate/up of this warp's first chunk does not depend on the
+        // accumulator: fetch it while the tile's MMAs run.
+        const uint32_t ord = bwd_chunk_order((j & 1) != 0, h, p.N - ti.nt * BN);
+        if ((ord >> 16) > 0) {
+          if (lane == 0) {
+            ptx::fence_proxy_async_smem();  // after the previous tile's reads of the boxes
+            load_gu(&tmC, ptx::smem_u32(gu_stage), bwd_col(ti, (int)(ord & 15)), p.F,
+                    (int)(ti.row0 + (long long)ti.mt * BM + q * 32), gu_bar);
+          }
+          gu_pending = true;
+        }
+      }
       if (!gemm::wait_bar(tfull_bar(j & 1), (uint32_t)((j >> 1) & 1), s_abort)) break;
       ptx::tc_fence_after();
       const bool odd = (j & 1) != 0;
@@ -612,12 +780,17 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(region_bar(1));
       epilogue_tile<MODE, EPI>(p, ti, odd, h, sh, tl_lanes + (odd ? (uint32_t)kAcc1Col : 0u), q,
-                               lane, xs, gu_stage, &tmC);
+                               lane, xs, gu_stage, &tmC, &tmQr, &tmQc, gu_bar, gu_phase,
+                               gu_pending, s_abort);
       ptx::tc_fence_before();
       ptx::mbar_arrive(region_bar(odd ? 2 : 0));
     }
-    // Bulk stores must be complete before this CTA's shared memory goes away.
-    if (EPI == EPI_SWIGLU_FWD && lane == 0) ptx::bulk_wait_all();
+    // Bulk stores must be complete, and a gate/up load left in flight by an
+    // abort must have landed, before this CTA's shared memory goes away.
+    if (EPI != EPI_STORE && lane == 0) {
+      ptx::bulk_wait_all();
+      if (gu_pending) gemm::drain_wait(gu_bar, gu_phase);
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -629,7 +802,8 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
 
 template <int MODE, int EPI>
 static int launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-                  const MxParams& p, long long tiles_bound, cudaStream_t st) {
+                  const CUtensorMap& tqr, const CUtensorMap& tqc, const MxParams& p,
+                  long long tiles_bound, cudaStream_t st) {
   using L = Cfg<EPI != EPI_STORE>;
   auto kern = grouped_gemm_mxf8_kernel<MODE, EPI>;
   static bool attr_set = false;
@@ -641,13 +815,20 @@ static int launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMa
   }
   long long grid = tiles_bound < gemm::num_sms() ? tiles_bound : gemm::num_sms();
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, L::kThreads, L::kSmemAlloc, st>>>(ta, tb, tc, p);
+  kern<<<(unsigned)grid, L::kThreads, L::kSmemAlloc, st>>>(ta, tb, tc, tqr, tqc, p);
   return launch_status();
 }
 
 static bool u8_map(CUtensorMap* m, const void* base, long long rows, long long cols) {
   // K-major E4M3 operand [rows, cols], box 128 rows x 128 bytes, 128B swizzle.
   return gemm::make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, cols, cols, 128, 128);
+}
+
+// Quantised epilogue output [rows, cols] (E4M3 codes), written in 32 x 32-byte
+// boxes staged with the 32-byte swizzle.
+static bool code_map(CUtensorMap* m, const void* base, long long rows, long long cols) {
+  return gemm::make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, cols, cols, 32, 32,
+                         CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
 }  // namespace gemm_mx
@@ -709,11 +890,11 @@ extern "C" int moe_grouped_gemm_mxfp8(int mode, const uint8_t* a, const uint8_t*
     p.b_row_stride = b_row_stride;
     p.b_k_stride = b_k_stride;
     long long bound = (a_rows / MX::BM + E) * (long long)((N + MX::BN - 1) / MX::BN);
-    return MX::launch<FPROP, EPI_STORE>(ta, tb, tb, p, bound, st);
+    return MX::launch<FPROP, EPI_STORE>(ta, tb, tb, tb, tb, p, bound, st);
   }
   p.c_group_stride = (long long)M * N;
   long long bound = (long long)E * (M / MX::BM) * (N / MX::BN);
-  return MX::launch<WGRAD, EPI_STORE>(ta, tb, tb, p, bound, st);
+  return MX::launch<WGRAD, EPI_STORE>(ta, tb, tb, tb, tb, p, bound, st);
 }
 
 extern "C" int moe_fc1_swiglu_mxfp8(const uint8_t* xq, const uint8_t* sx, long long rows, int H,
@@ -722,7 +903,8 @@ extern "C" int moe_fc1_swiglu_mxfp8(const uint8_t* xq, const uint8_t* sx, long l
                                     void* gu, uint8_t* hq_row, uint8_t* sh_row, uint8_t* hq_col,
                                     uint8_t* sh_col, moe_stream_t stream) {
   if (!mx_ptrs_ok(xq, sx, w1t, sw1t, gu) || !offsets || !p_rows || !hq_row || !sh_row ||
-      !hq_col || !sh_col || !aligned16(hq_row) || E < 1 || E > MX::kMaxGroups)
+      !hq_col || !sh_col || !aligned16(hq_row) || !aligned16(hq_col) || E < 1 ||
+      E > MX::kMaxGroups)
     return MOE_ERR_ARG;
   if (rows <= 0 || rows % 128 || rows >= (1LL << 31) || H < 128 || H % 128 || F < 128 || F % 128)
     return MOE_ERR_ARG;
@@ -747,15 +929,18 @@ extern "C" int moe_fc1_swiglu_mxfp8(const uint8_t* xq, const uint8_t* sx, long l
   p.q_col = hq_col;
   p.s_col = sh_col;
   p.q_col_ld = rows;
-  CUtensorMap ta, tb, tc;
+  CUtensorMap ta, tb, tc, tqr, tqc;
   if (!MX::u8_map(&ta, xq, rows, H) || !MX::u8_map(&tb, w1t, 2LL * F, (long long)E * H))
     return MOE_ERR_CUDA;
   // [g | u] output, written by TMA in 32 x 32 boxes
   if (!gemm::make_tmap(&tc, gu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, 2LL * F, 2LL * F, 32,
                        32, CU_TENSOR_MAP_SWIZZLE_NONE))
     return MOE_ERR_CUDA;
+  // H codes: row-wise [rows, F], column-wise [F, rows]
+  if (!MX::code_map(&tqr, hq_row, rows, F) || !MX::code_map(&tqc, hq_col, F, rows))
+    return MOE_ERR_CUDA;
   long long bound = (rows / MX::BM + E) * (long long)(F / 128);
-  return MX::launch<FPROP, EPI_SWIGLU_FWD>(ta, tb, tc, p, bound, (cudaStream_t)stream);
+  return MX::launch<FPROP, EPI_SWIGLU_FWD>(ta, tb, tc, tqr, tqc, p, bound, (cudaStream_t)stream);
 }
 
 extern "C" int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t* sdy2,
@@ -766,7 +951,8 @@ extern "C" int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t
                                               uint8_t* dy1q_col, uint8_t* sdy1_col,
                                               float* dp_part, moe_stream_t stream) {
   if (!mx_ptrs_ok(dy2q, sdy2, w2q, sw2, gu) || !offsets || !p_rows || !dy1q_row || !sdy1_row ||
-      !dy1q_col || !sdy1_col || !dp_part || !aligned16(dy1q_row) || E < 1 || E > MX::kMaxGroups)
+      !dy1q_col || !sdy1_col || !dp_part || !aligned16(dy1q_row) || !aligned16(dy1q_col) ||
+      E < 1 || E > MX::kMaxGroups)
     return MOE_ERR_ARG;
   if (rows <= 0 || rows % 128 || rows >= (1LL << 31) || H < 128 || H % 128 || F < 128 || F % 128)
     return MOE_ERR_ARG;
@@ -793,8 +979,15 @@ extern "C" int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t
   p.q_col_ld = rows;
   p.dp_part = dp_part;
   p.n_part = 2 * ((F + MX::BN - 1) / MX::BN);  // two epilogue warps per row and tile
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tgu, tqr, tqc;
   if (!MX::u8_map(&ta, dy2q, rows, H) || !MX::u8_map(&tb, w2q, (long long)E * F, H)) return MOE_ERR_CUDA;
+  // saved [g | u], read by TMA in 32 x 32 boxes with the 64-byte swizzle
+  if (!gemm::make_tmap(&tgu, gu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, 2LL * F, 2LL * F, 32,
+                       32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return MOE_ERR_CUDA;
+  // dY1 codes: row-wise [rows, 2F], column-wise [2F, rows]
+  if (!MX::code_map(&tqr, dy1q_row, rows, 2LL * F) || !MX::code_map(&tqc, dy1q_col, 2LL * F, rows))
+    return MOE_ERR_CUDA;
   long long bound = (rows / MX::BM + E) * (long long)((F + MX::BN - 1) / MX::BN);
-  return MX::launch<FPROP, EPI_SWIGLU_BWD>(ta, tb, tb, p, bound, (cudaStream_t)stream);
+  return MX::launch<FPROP, EPI_SWIGLU_BWD>(ta, tb, tgu, tqr, tqc, p, bound, (cudaStream_t)stream);
 }
