@@ -67,12 +67,14 @@ struct Params {
   int n_part;
 };
 
-template <int BN>
+// CG = 2: a CTA pair shares each tile (M = 256), each CTA staging its own 128
+// rows of A and half of the B columns, so a stage is 32 KB instead of 48.
+template <int BN, int CG = 1>
 struct Smem {
   static constexpr int kABytes = BM * BK * 2;
-  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kBBytes = (BN / CG) * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = (BN == 256) ? 4 : 6;
+  static constexpr int kStages = (CG == 2 || BN != 256) ? 6 : 4;
   static constexpr int kBarOffset = kStages * kStageBytes;
   // full[S], empty[S], tfull[2], tempty[2], drain
   static constexpr int kNumBars = 2 * kStages + 5;
@@ -116,9 +118,10 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <int MODE, int BN>
+template <int MODE, int BN, int CG>
 __device__ __forceinline__ void decode_tile(const Params& p, const int* prefix, int t, int& e_hint,
                                             TileInfo& ti) {
+  constexpr int kTileM = BM * CG;
   int e = e_hint;
   while (prefix[e + 1] <= t) ++e;
   e_hint = e;
@@ -128,12 +131,12 @@ __device__ __forceinline__ void decode_tile(const Params& p, const int* prefix, 
   ti.row0 = o0;
   ti.rows = (int)(o1 - o0);
   if (MODE == FPROP) {
-    const int mtiles = (ti.rows + BM - 1) / BM;
+    const int mtiles = (ti.rows + kTileM - 1) / kTileM;
     ti.mt = local % mtiles;
     ti.nt = local / mtiles;
     ti.k_iters = p.K / BK;
   } else {
-    const int mtiles = p.M / BM;
+    const int mtiles = p.M / kTileM;
     ti.mt = local % mtiles;
     ti.nt = local / mtiles;
     ti.k_iters = ti.rows / BK;
@@ -188,11 +191,15 @@ __device__ __forceinline__ float sigmoidf_fast(float z) {
   return r;
 }
 
-template <int MODE, int EPI, int BN, int A_MN, int B_MN>
+template <int MODE, int EPI, int BN, int A_MN, int B_MN, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB, const Params p) {
-  using L = Smem<BN>;
+  using L = Smem<BN, CG>;
+  constexpr bool kPair = CG == 2;
+  // Rows of A (and columns of B) this CTA stages per stage, and the tile's M.
+  constexpr int kTileM = BM * CG;
+  constexpr int kBCols = BN / CG;  // this CTA's share of the tile's B columns
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -209,6 +216,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = p.N / BN;
+  // CTA pairs: rank 0 (the leader) issues the MMAs; tiles are dealt out per pair.
+  const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
+  const int unit = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int n_units = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::kStages; ++s) {
@@ -217,7 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(tfull_bar(b), 1);
-      ptx::mbar_init(tempty_bar(b), 128);
+      // single CTA: every epilogue thread arrives; pair: one arrival per
+      // epilogue warp of both CTAs, on the leader's barrier
+      ptx::mbar_init(tempty_bar(b), kPair ? 8 : 128);
     }
     ptx::mbar_init(drain_bar, 1);
     ptx::fence_mbar_init();
@@ -230,9 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int rows = p.offsets[e + 1] - p.offsets[e];
       int mt;
       if (MODE == FPROP) {
-        mt = (rows + BM - 1) / BM;
+        mt = (rows + kTileM - 1) / kTileM;
       } else {
-        mt = p.M / BM;
+        mt = p.M / kTileM;
         if (rows % BK) bad = true;
       }
       acc += mt * n_tiles;
@@ -245,11 +258,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(s_tmem), 2 * BN);
-    ptx::tmem_relinquish();
+    if (kPair) {
+      ptx::tmem_alloc_cg2(ptx::smem_u32(s_tmem), 2 * BN);
+      ptx::tmem_relinquish_cg2();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(s_tmem), 2 * BN);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  // A pair's barriers must be initialised in both CTAs before either CTA's
+  // copies, commits or arrivals can reach them.
+  if (kPair)
+    ptx::cluster_sync();
+  else
+    __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
   const int total_tiles = s_prefix[p.E];
@@ -264,9 +287,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < L::kStages; ++s) armed[s] = false;
       int e_hint = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      for (int t = unit; t < total_tiles && ok; t += n_units) {
         TileInfo ti;
-        decode_tile<MODE, BN>(p, s_prefix, t, e_hint, ti);
+        decode_tile<MODE, BN, CG>(p, s_prefix, t, e_hint, ti);
         for (int kb = 0; kb < ti.k_iters; ++kb) {
           if (!wait_bar(empty_bar(stage), phase ^ 1u, s_abort)) {
             ok = false;
@@ -274,30 +297,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t a_dst = sbase + stage * L::kStageBytes;
           const uint32_t b_dst = a_dst + L::kABytes;
-          ptx::mbar_arrive_expect_tx(full_bar(stage), L::kStageBytes);
-          armed[stage] = true;
-          armed_phase[stage] = phase;
+          // Completion of both CTAs' copies of a pair is counted on the leader's barrier.
+          const uint32_t fb = kPair ? ptx::mapa_shared(full_bar(stage), 0) : full_bar(stage);
+          if (rank == 0) {
+            ptx::mbar_arrive_expect_tx(full_bar(stage), CG * L::kStageBytes);
+            armed[stage] = true;
+            armed_phase[stage] = phase;
+          }
+          auto load = [&](uint32_t dst, const CUtensorMap* tm, int c0, int c1) {
+            if (kPair)
+              ptx::tma_load_2d_cg2(dst, tm, c0, c1, fb);
+            else
+              ptx::tma_load_2d(dst, tm, c0, c1, fb);
+          };
           const int k0 = kb * BK;
           if (MODE == FPROP) {
-            // A: rows of the group, K-major, one box of 128 rows x BK.
-            ptx::tma_load_2d(a_dst, &tmA, k0, (int)(ti.row0 + (long long)ti.mt * BM),
-                             full_bar(stage));
+            // A: this CTA's 128 rows of the tile, K-major, one box of 128 rows x BK.
+            load(a_dst, &tmA, k0, (int)(ti.row0 + (long long)ti.mt * kTileM + rank * BM));
             if (B_MN) {
-              // B_e stored [K, N]: BN/64 chunks of [BK K rows][64 N].
+              // B_e stored [K, N]: this CTA's kBCols columns as chunks of [BK K rows][64 N].
 #pragma unroll
-              for (int c = 0; c < BN / 64; ++c) {
-                const int h = c / (BN / 128), off = (c % (BN / 128)) * 64;
+              for (int c = 0; c < kBCols / 64; ++c) {
+                const int cc = (int)rank * (kBCols / 64) + c;  // chunk of the whole tile
+                const int h = cc / (BN / 128), off = (cc % (BN / 128)) * 64;
                 const int n = b_half_col<EPI, BN>(p, ti.nt, h) + off;
-                ptx::tma_load_2d(b_dst + c * (BK * 128), &tmB, n, ti.e * p.K + k0,
-                                 full_bar(stage));
+                load(b_dst + c * (BK * 128), &tmB, n, ti.e * p.K + k0);
               }
             } else {
-              // B_e stored [N, K]: two boxes of BN/2 rows x BK.
+              // B_e stored [N, K]: boxes of BN/2 rows x BK (one per CTA of a pair).
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const int n = b_half_col<EPI, BN>(p, ti.nt, h);
-                ptx::tma_load_2d(b_dst + h * (BN / 2) * kKRowBytes, &tmB, k0, ti.e * p.N + n,
-                                 full_bar(stage));
+              for (int h = 0; h < 2 / CG; ++h) {
+                const int n = b_half_col<EPI, BN>(p, ti.nt, kPair ? (int)rank : h);
+                load(b_dst + h * (BN / 2) * kKRowBytes, &tmB, k0, ti.e * p.N + n);
               }
             }
           } else {
@@ -305,12 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r = (int)(ti.row0 + k0);
 #pragma unroll
             for (int c = 0; c < BM / 64; ++c)
-              ptx::tma_load_2d(a_dst + c * (BK * 128), &tmA, ti.mt * BM + c * 64, r,
-                               full_bar(stage));
+              load(a_dst + c * (BK * 128), &tmA, ti.mt * kTileM + (int)rank * BM + c * 64, r);
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-              ptx::tma_load_2d(b_dst + c * (BK * 128), &tmB, ti.nt * BN + c * 64, r,
-                               full_bar(stage));
+            for (int c = 0; c < kBCols / 64; ++c)
+              load(b_dst + c * (BK * 128), &tmB, ti.nt * BN + (int)rank * kBCols + c * 64, r);
           }
           if (++stage == L::kStages) {
             stage = 0;
@@ -318,23 +347,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // Let every armed copy land before the CTA can exit (bounded).
+      // Let every armed copy land before the CTA can exit (bounded). The
+      // leader's barriers count both CTAs' copies of a pair.
       for (int s = 0; s < L::kStages; ++s)
         if (armed[s]) drain_wait(full_bar(s), armed_phase[s]);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
-    if (ptx::elect_one()) {
-      constexpr uint32_t idesc = ptx::idesc_bf16(BM, BN, MODE == WGRAD ? 1 : A_MN, B_MN);
+    if (rank == 0 && ptx::elect_one()) {
+      constexpr uint32_t idesc = ptx::idesc_bf16(kTileM, BN, MODE == WGRAD ? 1 : A_MN, B_MN);
+      constexpr uint16_t kBoth = 3;  // commit to the barrier of both CTAs of a pair
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       int e_hint = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      for (int t = unit; t < total_tiles && ok; t += n_units) {
         TileInfo ti;
-        decode_tile<MODE, BN>(p, s_prefix, t, e_hint, ti);
+        decode_tile<MODE, BN, CG>(p, s_prefix, t, e_hint, ti);
         if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, s_abort)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -357,45 +388,62 @@ __global__ void __launch_bounds__(kThreads, 1)
               db = ptx::smem_desc(b_addr + kk * 2048, BK * 128, 1024, ptx::kSwizzle128B);
             else
               db = ptx::smem_desc(b_addr + kk * 32, 16, kKAtomBytes, ptx::kSwizzle128B);
-            ptx::mma_bf16(d_tmem, da, db, idesc, (kb | kk) ? 1u : 0u);
+            if (kPair)
+              ptx::mma_bf16_cg2(d_tmem, da, db, idesc, (kb | kk) ? 1u : 0u);
+            else
+              ptx::mma_bf16(d_tmem, da, db, idesc, (kb | kk) ? 1u : 0u);
           }
-          ptx::mma_commit(empty_bar(stage));
+          if (kPair)
+            ptx::mma_commit_cg2(empty_bar(stage), kBoth);
+          else
+            ptx::mma_commit(empty_bar(stage));
           if (++stage == L::kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        if (ti.k_iters > 0)
-          ptx::mma_commit(tfull_bar(acc));
-        else
+        if (ti.k_iters > 0) {
+          if (kPair)
+            ptx::mma_commit_cg2(tfull_bar(acc), kBoth);
+          else
+            ptx::mma_commit(tfull_bar(acc));
+        } else {
           ptx::mbar_arrive(tfull_bar(acc));
+          if (kPair) ptx::mbar_arrive_remote(ptx::mapa_shared(tfull_bar(acc), 1));
+        }
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
       // All MMAs issued by this thread complete before TMEM is released.
-      ptx::mma_commit(drain_bar);
+      if (kPair)
+        ptx::mma_commit_cg2(drain_bar, 1);
+      else
+        ptx::mma_commit(drain_bar);
       drain_wait(drain_bar, 0);
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int r = q * 32 + lane;  // row of the tile
+    const int r = q * 32 + lane;  // row of this CTA's part of the tile
+    // The accumulator-free arrival goes to the leader's barrier (one per warp
+    // for a pair).
     int acc = 0;
     uint32_t acc_phase = 0;
     int e_hint = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+    for (int t = unit; t < total_tiles; t += n_units) {
       TileInfo ti;
-      decode_tile<MODE, BN>(p, s_prefix, t, e_hint, ti);
+      decode_tile<MODE, BN, CG>(p, s_prefix, t, e_hint, ti);
       if (!wait_bar(tfull_bar(acc), acc_phase, s_abort)) break;
       ptx::tc_fence_after();
       const uint32_t tm = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       const bool has_acc = ti.k_iters > 0;
+      const int mrow = ti.mt * kTileM + (int)rank * BM + r;  // row of the group's tile rows
       if (MODE == WGRAD) {
         __nv_bfloat16* crow = p.C + (long long)ti.e * p.c_group_stride +
-                              (long long)(ti.mt * BM + r) * p.ldc + (long long)ti.nt * BN;
+                              (long long)mrow * p.ldc + (long long)ti.nt * BN;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
@@ -412,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           store32_bf16(crow + c * 32, f);
         }
       } else {
-        const int lrow = ti.mt * BM + r;
+        const int lrow = mrow;
         const bool row_ok = lrow < ti.rows;
         const long long grow = ti.row0 + lrow;
         if (EPI == EPI_STORE) {
@@ -484,7 +532,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(tempty_bar(acc));
+      if (kPair) {
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0)
+            ptx::mbar_arrive(tempty_bar(acc));
+          else
+            ptx::mbar_arrive_remote(ptx::mapa_shared(tempty_bar(acc), 0));
+        }
+      } else {
+        ptx::mbar_arrive(tempty_bar(acc));
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -492,10 +550,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  // A pair leaves together: the leader's MMAs write the peer's tensor memory
+  // and the peer's copies and arrivals reach the leader's barriers.
+  if (kPair)
+    ptx::cluster_sync();
+  else
+    __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, 2 * BN);
+    if (kPair)
+      ptx::tmem_dealloc_cg2(tmem_base, 2 * BN);
+    else
+      ptx::tmem_dealloc(tmem_base, 2 * BN);
   }
 }
 
@@ -517,21 +584,57 @@ static int num_sms() {
   return n;
 }
 
-template <int MODE, int EPI, int BN, int A_MN, int B_MN>
+// tiles_bound: an upper bound on the tiles of the launch (for CG = 2, on the
+// 256-row tiles that CTA pairs take).
+template <int MODE, int EPI, int BN, int A_MN, int B_MN, int CG = 1>
 static int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
                   long long tiles_bound, cudaStream_t st) {
-  auto kern = grouped_gemm_bf16_kernel<MODE, EPI, BN, A_MN, B_MN>;
-  const int smem = Smem<BN>::kAlloc;
+  auto kern = grouped_gemm_bf16_kernel<MODE, EPI, BN, A_MN, B_MN, CG>;
+  const int smem = Smem<BN, CG>::kAlloc;
   static bool attr_set = false;
+  static int max_units = 0;  // co-resident CTAs (CG = 1) or CTA pairs (CG = 2)
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
+    max_units = num_sms();
+    if (CG == 2) {
+      cudaLaunchConfig_t q = {};
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = 2;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      q.gridDim = dim3(2 * (num_sms() / 2));
+      q.blockDim = dim3(kThreads);
+      q.dynamicSmemBytes = smem;
+      q.attrs = qa;
+      q.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n < 1) return MOE_ERR_CUDA;
+      max_units = n;
+    }
     attr_set = true;
   }
-  long long grid = tiles_bound < num_sms() ? tiles_bound : num_sms();
-  if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, kThreads, smem, st>>>(ta, tb, p);
+  long long units = tiles_bound < max_units ? tiles_bound : max_units;
+  if (units < 1) units = 1;
+  if (CG == 1) {
+    kern<<<(unsigned)units, kThreads, smem, st>>>(ta, tb, p);
+    return launch_status();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(2 * units));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, p) != cudaSuccess) return MOE_ERR_CUDA;
   return launch_status();
 }
 
@@ -579,8 +682,8 @@ extern "C" int moe_grouped_gemm_bf16(int mode, const void* A, const void* B, int
     }
     long long bound = (rows / BM + E) * (long long)(N / 128);
     if (bn256)
-      return b_layout ? launch<FPROP, EPI_STORE, 256, 0, 0>(ta, tb, p, bound, st)
-                      : launch<FPROP, EPI_STORE, 256, 0, 1>(ta, tb, p, bound, st);
+      return b_layout ? launch<FPROP, EPI_STORE, 256, 0, 0, 2>(ta, tb, p, bound, st)
+                      : launch<FPROP, EPI_STORE, 256, 0, 1, 2>(ta, tb, p, bound, st);
     return b_layout ? launch<FPROP, EPI_STORE, 128, 0, 0>(ta, tb, p, bound, st)
                     : launch<FPROP, EPI_STORE, 128, 0, 1>(ta, tb, p, bound, st);
   }
@@ -598,6 +701,7 @@ extern "C" int moe_grouped_gemm_bf16(int mode, const void* A, const void* B, int
       tb = ta;
     }
     long long bound = (long long)E * (M / BM) * (N / 128);
+    if (bn256 && M % 256 == 0) return launch<WGRAD, EPI_STORE, 256, 1, 1, 2>(ta, tb, p, bound, st);
     return bn256 ? launch<WGRAD, EPI_STORE, 256, 1, 1>(ta, tb, p, bound, st)
                  : launch<WGRAD, EPI_STORE, 128, 1, 1>(ta, tb, p, bound, st);
   }
@@ -625,7 +729,7 @@ extern "C" int moe_fc1_swiglu_bf16(const void* xp, const void* w1, const int32_t
   long long bound_base = rows / BM + E;
   cudaStream_t st = (cudaStream_t)stream;
   if (F % 128 == 0)
-    return launch<FPROP, EPI_SWIGLU_FWD, 256, 0, 1>(ta, tb, p, bound_base * (F / 128), st);
+    return launch<FPROP, EPI_SWIGLU_FWD, 256, 0, 1, 2>(ta, tb, p, bound_base * (F / 128), st);
   return launch<FPROP, EPI_SWIGLU_FWD, 128, 0, 1>(ta, tb, p, bound_base * (F / 64), st);
 }
 
@@ -662,6 +766,6 @@ extern "C" int moe_fc2_dgrad_swiglu_bwd_bf16(const void* dy2, const void* w2,
     return MOE_ERR_CUDA;
   long long bound = (rows / BM + E) * (long long)(F / 128);
   cudaStream_t st = (cudaStream_t)stream;
-  return bn256 ? launch<FPROP, EPI_SWIGLU_BWD, 256, 0, 0>(ta, tb, p, bound, st)
+  return bn256 ? launch<FPROP, EPI_SWIGLU_BWD, 256, 0, 0, 2>(ta, tb, p, bound, st)
                : launch<FPROP, EPI_SWIGLU_BWD, 128, 0, 0>(ta, tb, p, bound, st);
 }
