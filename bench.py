@@ -239,7 +239,8 @@ class Step:
                                                       *q("w2"), s)),
                 ("fc1_swiglu", lambda: L.moe_fc1_swiglu_mxfp8(
                     p(P["x_q_row"]), p(P["x_s_row"]), R, H, p(P["w1_q_col"]), p(P["w1_s_col"]),
-                    p(P["offsets"]), p(P["p_rows"]), E, F, p(P["gu"]), *q("h"), s)),
+                    p(P["offsets"]), p(P["p_rows"]), E, F, p(P["gu"]),
+                    *(q("h")[:2] + ([None, None] if self.act4 else q("h")[2:])), s)),
             ]
             if self.act4:
                 ops += [("x_to_fp4", to_fp4("x", H)), ("h_to_fp4", to_fp4("h", F))]

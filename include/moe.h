@@ -412,7 +412,8 @@ MOE_API int moe_grouped_gemm_mxfp8(int mode, const uint8_t* a, const uint8_t* sa
  *   For every row r of group e: [g | u] = x_r * W1_e (fp32),
  *   gu[r] = [g | u] in bf16, h = silu(g)*u*p_rows[r] (fp32), written as
  *   row-wise MXFP8 hq_row [rows, F] + sh_row and column-wise MXFP8 (blocks of
- *   32 rows, transposed) hq_col [F, rows] + sh_col.
+ *   32 rows, transposed) hq_col [F, rows] + sh_col. hq_col and sh_col may
+ *   both be NULL: then no column-wise copy is computed or written.
  * Requires rows, H, F multiples of 128. */
 MOE_API int moe_fc1_swiglu_mxfp8(const uint8_t* xq, const uint8_t* sx, long long rows, int H,
                                  const uint8_t* w1t, const uint8_t* sw1t, const int32_t* offsets,
@@ -471,7 +472,13 @@ MOE_API int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t* s
  *     (mxfp4_from_mxfp8). The backward rebuilds their column-wise MXFP8
  *     operands with mxfp8_colwise_from_mxfp4_rowwise before the two wgrad
  *     GEMMs, so dW1 and dW2 see X and H quantised FP8 -> FP4 -> column-wise
- *     FP4; the column-wise FP8 parts of X and H serve as scratch.
+ *     FP4. The row-wise FP8 copies of X and H are dead after the forward, so
+ *     in this mode the column-wise FP8 parts of X and H occupy the same bytes
+ *     as their row-wise parts (moe_layer_workspace_part reports the same
+ *     offsets): after the backward, those bytes hold the rebuilt column-wise
+ *     copies. The forward writes no column-wise H. The workspace is therefore
+ *     smaller than in MXFP8 mode by one FP8 copy of X and of H, less their
+ *     MXFP4 copies.
  * Requirements: H % 128 == 0 (H % 256 == 0 for MXFP8), F % 128 == 0,
  * 1 <= k <= 8, k <= E <= 256, align a multiple of 128 (groups are padded with
  * zero rows). moe_layer_workspace_size returns 0 for an unsupported cfg. The

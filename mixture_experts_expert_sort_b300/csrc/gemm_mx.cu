@@ -329,20 +329,22 @@ __device__ __forceinline__ void fwd_pair(const MxParams& p, const TileInfo& ti, 
   }
 #pragma unroll
   for (int i = 0; i < 32; ++i) g[i] = g[i] * gemm::sigmoidf_fast(g[i]) * u[i] * pr;  // h
-  // H: the column-wise block through the transpose, then the row-wise block.
+  // H: the column-wise block through the transpose (unless the caller wants
+  // no column-wise copy), then the row-wise block.
+  const bool cols = p.q_col != nullptr;
   uint32_t wc[8], wr[8];
-  quant_col32(g, wc, p.s_col, p.q_col_ld, col, rb, xs, lane);
+  if (cols) quant_col32(g, wc, p.s_col, p.q_col_ld, col, rb, xs, lane);
   const uint32_t sb = quant32(g, wr);
   if (row_ok) p.s_row[mx_scale_offset(grow, col >> 5, p.q_row_ld)] = (uint8_t)sb;
   __syncwarp();  // every lane has read its column out of the buffer
   stage_codes(xb, lane, wr);
-  stage_codes(xb + 1024, lane, wc);
+  if (cols) stage_codes(xb + 1024, lane, wc);
   ptx::fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
     const uint32_t xb_s = ptx::smem_u32(xb);
     ptx::tma_store_2d(tm_qr, (int)col, (int)rb, xb_s);
-    ptx::tma_store_2d(tm_qc, (int)rb, (int)col, xb_s + 1024);
+    if (cols) ptx::tma_store_2d(tm_qc, (int)rb, (int)col, xb_s + 1024);
     ptx::bulk_commit_group();
   }
 }
@@ -902,9 +904,10 @@ extern "C" int moe_fc1_swiglu_mxfp8(const uint8_t* xq, const uint8_t* sx, long l
                                     const int32_t* offsets, const float* p_rows, int E, int F,
                                     void* gu, uint8_t* hq_row, uint8_t* sh_row, uint8_t* hq_col,
                                     uint8_t* sh_col, moe_stream_t stream) {
+  // The column-wise copy of H is optional (both pointers NULL: not written).
   if (!mx_ptrs_ok(xq, sx, w1t, sw1t, gu) || !offsets || !p_rows || !hq_row || !sh_row ||
-      !hq_col || !sh_col || !aligned16(hq_row) || !aligned16(hq_col) || E < 1 ||
-      E > MX::kMaxGroups)
+      (hq_col == nullptr) != (sh_col == nullptr) || !aligned16(hq_row) || !aligned16(hq_col) ||
+      E < 1 || E > MX::kMaxGroups)
     return MOE_ERR_ARG;
   if (rows <= 0 || rows % 128 || rows >= (1LL << 31) || H < 128 || H % 128 || F < 128 || F % 128)
     return MOE_ERR_ARG;
@@ -936,8 +939,10 @@ extern "C" int moe_fc1_swiglu_mxfp8(const uint8_t* xq, const uint8_t* sx, long l
   if (!gemm::make_tmap(&tc, gu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, 2LL * F, 2LL * F, 32,
                        32, CU_TENSOR_MAP_SWIZZLE_NONE))
     return MOE_ERR_CUDA;
-  // H codes: row-wise [rows, F], column-wise [F, rows]
-  if (!MX::code_map(&tqr, hq_row, rows, F) || !MX::code_map(&tqc, hq_col, F, rows))
+  // H codes: row-wise [rows, F], column-wise [F, rows] (the row-wise map
+  // stands in when there is no column-wise copy; it is then never used)
+  if (!MX::code_map(&tqr, hq_row, rows, F) ||
+      !MX::code_map(&tqc, hq_col ? hq_col : hq_row, hq_col ? F : rows, hq_col ? rows : F))
     return MOE_ERR_CUDA;
   long long bound = (rows / MX::BM + E) * (long long)(F / 128);
   return MX::launch<FPROP, EPI_SWIGLU_FWD>(ta, tb, tc, tqr, tqc, p, bound, (cudaStream_t)stream);

@@ -115,10 +115,25 @@ static Layout layout(const moe_layer_config* c) {
   L.bytes[P_X4S] = a4 * mx_scale_bytes(R, H);
   L.bytes[P_H4Q] = a4 * R * F / 2;
   L.bytes[P_H4S] = a4 * mx_scale_bytes(R, F);
+  // MXFP4-activation mode: x and H reach the backward only as their MXFP4
+  // copies. Their row-wise FP8 copies are dead once the forward is done, so
+  // the column-wise FP8 operands the backward rebuilds for the two wgrads
+  // take the same bytes (a [cols, rows] copy has the size of its [rows, cols]
+  // one, scales included), and the forward writes no column-wise H.
+  auto aliased = [&](int i) {
+    return a4 && (i == P_XQ_COL || i == P_XS_COL || i == P_HQ_COL || i == P_HS_COL);
+  };
   size_t o = 0;
   for (int i = 0; i < P_COUNT; ++i) {
+    if (aliased(i)) continue;
     L.off[i] = o;
     o += up256(L.bytes[i]);
+  }
+  if (a4) {
+    L.off[P_XQ_COL] = L.off[P_XQ_ROW];
+    L.off[P_XS_COL] = L.off[P_XS_ROW];
+    L.off[P_HQ_COL] = L.off[P_HQ_ROW];
+    L.off[P_HS_COL] = L.off[P_HS_ROW];
   }
   L.total = o;
   return L;
@@ -185,9 +200,11 @@ extern "C" int moe_layer_forward(const moe_layer_config* cfg, const float* logit
     MOE_TRY(mxfp8_quantize(w2, (long long)E * F, H, H, nullptr, 1,
                            MOE_QUANT_ROWWISE | MOE_QUANT_COLWISE, P(P_W2Q_ROW), P(P_W2S_ROW),
                            P(P_W2Q_COL), P(P_W2S_COL), stream));
+    // ACT4: no column-wise H (its bytes are the row-wise H that FC2 reads)
     MOE_TRY(moe_fc1_swiglu_mxfp8(P(P_XQ_ROW), P(P_XS_ROW), R, H, P(P_W1Q_COL), P(P_W1S_COL),
                                  offsets, p_rows, E, F, P(P_GU), P(P_HQ_ROW), P(P_HS_ROW),
-                                 P(P_HQ_COL), P(P_HS_COL), stream));
+                                 is_act4(cfg) ? nullptr : P(P_HQ_COL),
+                                 is_act4(cfg) ? nullptr : P(P_HS_COL), stream));
     if (is_act4(cfg))  // H is carried to the backward as MXFP4
       MOE_TRY(mxfp4_from_mxfp8(P(P_HQ_ROW), P(P_HS_ROW), R, F, P(P_H4Q), P(P_H4S), stream));
     // FC2: B_e[n, f] = W2_e[f, n] from the column-wise copy [H, E*F] (blocks along F)
@@ -234,7 +251,8 @@ extern "C" int moe_layer_backward(const moe_layer_config* cfg, const void* dout,
                                            P(P_W2S_ROW), offsets, p_rows, P(P_GU), E, F,
                                            P(P_DY1Q_ROW), P(P_DY1S_ROW), P(P_DY1Q_COL),
                                            P(P_DY1S_COL), dp, stream));
-    // ACT4: the column-wise operands of the two wgrads come from the MXFP4 copies
+    // ACT4: the column-wise operands of the two wgrads come from the MXFP4
+    // copies, into the bytes of the (now dead) row-wise FP8 copies
     if (is_act4(cfg)) {
       MOE_TRY(mxfp8_colwise_from_mxfp4_rowwise(P(P_H4Q), P(P_H4S), R, F, P(P_HQ_COL), P(P_HS_COL),
                                                stream));

@@ -62,10 +62,12 @@ def test_mxfp4_argument_checks(libmoe):
 
 
 def test_layer_workspace_layouts(libmoe):
-    """Host-only layout queries: the MXFP4-activation mode adds exactly the
-    row-wise MXFP4 copies of x and H (half a byte per element plus scales) to
-    the MXFP8 layout; parts of another precision have size 0; unsupported
-    configs report size 0 (H % 256 for the MXFP8 modes, align % 128)."""
+    """Host-only layout queries: the MXFP4-activation mode adds the row-wise
+    MXFP4 copies of x and H (half a byte per element plus scales) to the
+    MXFP8 layout and keeps their column-wise FP8 copies in the bytes of the
+    row-wise ones, which the backward no longer needs; parts of another
+    precision have size 0; unsupported configs report size 0 (H % 256 for
+    the MXFP8 modes, align % 128)."""
     from mixture_experts_expert_sort_b300 import binding as B
     T, H, F, E, k = 16384, 4096, 14336, 8, 2
     c8 = B.layer_config(T, H, F, E, k, "mxfp8")
@@ -76,7 +78,19 @@ def test_layer_workspace_layouts(libmoe):
     scale = lambda mn, kd: (mn // 128) * (kd // 128) * 512  # noqa: E731
     extra = [R * H // 2, scale(R, H), R * F // 2, scale(R, F)]
     up = lambda b: -(-b // 256) * 256  # noqa: E731
-    assert B.moe_layer_workspace_size(c4) == B.moe_layer_workspace_size(c8) + sum(map(up, extra))
+    fp8 = [R * H, scale(H, R), R * F, scale(F, R)]  # the column-wise FP8 copies of x and H
+    assert B.moe_layer_workspace_size(c4) == (B.moe_layer_workspace_size(c8) + sum(map(up, extra))
+                                              - sum(map(up, fp8)))
+    # at this (Mixtral, T = 16384) shape the mode saves about 311 MB of workspace
+    saved = B.moe_layer_workspace_size(c8) - B.moe_layer_workspace_size(c4)
+    assert 305e6 < saved < 315e6, saved
+    for row, col in (("x_q_row", "x_q_col"), ("x_s_row", "x_s_col"), ("h_q_row", "h_q_col"),
+                     ("h_s_row", "h_s_col")):
+        r_off, r_bytes = B.moe_layer_workspace_part(c4, B.PARTS[row][0])
+        c_off, c_bytes = B.moe_layer_workspace_part(c4, B.PARTS[col][0])
+        assert (r_off, r_bytes) == (c_off, c_bytes), (row, col)
+        assert B.moe_layer_workspace_part(c8, B.PARTS[row][0])[0] != \
+            B.moe_layer_workspace_part(c8, B.PARTS[col][0])[0]
     for name, want in zip(("x4_q_row", "x4_s_row", "h4_q_row", "h4_s_row"), extra):
         part = B.PARTS[name][0]
         assert B.moe_layer_workspace_part(c4, part)[1] == want, name

@@ -23,12 +23,18 @@ DEV = "cuda"
 TOL_MX = 1e-2
 
 
-def _run(wl, inp, precision="mxfp8"):
+def _run(wl, inp, precision="mxfp8", after_forward=None):
+    """Forward and backward; after_forward(L) inspects the workspace between
+    the two (in the MXFP4-activation mode the backward reuses the bytes of
+    the forward's row-wise FP8 copies of x and H)."""
     from mixture_experts_expert_sort_b300 import binding
     from mixture_experts_expert_sort_b300.layer import MoELayer
     L = MoELayer(wl.T, wl.H, wl.F, wl.E, wl.k, precision=precision, align=wl.align)
     d = {k: v.to(DEV) for k, v in inp.items()}
     out = L.forward(d["logits"], d["x"], d["w1"], d["w2"])
+    if after_forward is not None:
+        torch.cuda.synchronize()
+        after_forward(L)
     dx, dw1, dw2, dl = L.backward(d["dout"], d["w1"], d["w2"])
     torch.cuda.synchronize()
     assert binding.device_error() == 0
@@ -79,7 +85,8 @@ def _check_colwise(L, name, mn, kd, blocks, block_vals):
 
 def _check_input_quantisation(L, wl, inp, n_rows=None, n_blocks=None, seed=0, act4=False):
     """Bit-exact MXFP8 of the gathered x and dOut and of both weights (in the
-    MXFP4 activation mode the column-wise x is checked by _check_act4_x)."""
+    MXFP4 activation mode x is checked by _check_act4_x_forward and
+    _check_act4_x instead)."""
     rng = np.random.default_rng(seed)
     src, R = _rows_of(L, wl)
     k = wl.k
@@ -88,11 +95,11 @@ def _check_input_quantisation(L, wl, inp, n_rows=None, n_blocks=None, seed=0, ac
         return np.arange(n) if m is None or m >= n else np.sort(rng.choice(n, m, replace=False))
 
     for name, t in (("x", inp["x"]), ("dy2", inp["dout"])):
+        if act4 and name == "x":
+            continue
         x = t.float().numpy()
         rows = pick(R, n_rows)
         _check_rowwise(L, name, R, wl.H, rows, _gathered(x, src, k, rows))
-        if act4 and name == "x":
-            continue
         blocks = pick(R // 32, n_blocks)
         _check_colwise(L, name, R, wl.H, blocks,
                        [_gathered(x, src, k, np.arange(32 * b, 32 * b + 32)) for b in blocks])
@@ -190,17 +197,28 @@ def _sampled_parity(wl, n_tokens=256):
         assert not torch.any(g["dW1"][int(e)]) and not torch.any(g["dW2"][int(e)])
 
 
+def _check_act4_x_forward(L, wl, inp):
+    """MXFP4 activation mode after the forward, bit-exact: the row-wise MXFP8
+    of the gathered x that FC1 read, and the MXFP4 copy made from it."""
+    from oracle import mxfp4_oracle as Q
+    src, R = _rows_of(L, wl)
+    xg = _gathered(inp["x"].float().numpy(), src, wl.k, np.arange(R))
+    _check_rowwise(L, "x", R, wl.H, np.arange(R), xg)
+    c4, s4 = Q.mxfp4_from_mxfp8(*O.mx_quantize(xg, axis=1))
+    np.testing.assert_array_equal(u8(L.part("x4_q_row")).reshape(R, wl.H // 2), Q.pack_e2m1(c4))
+    np.testing.assert_array_equal(
+        scales_tiled_to_rowmajor(u8(L.part("x4_s_row")), R, wl.H), s4)
+
+
 def _check_act4_x(L, wl, inp):
-    """MXFP4 activation mode, bit-exact on the input side: the saved MXFP4 copy
-    of the gathered x (FP8 -> FP4 of its row-wise MXFP8) and the column-wise
-    MXFP8 operand the backward rebuilt from it."""
+    """MXFP4 activation mode after the backward, bit-exact: the column-wise
+    MXFP8 operand of FC1's wgrad that the backward rebuilt from the MXFP4
+    copy of x (in the bytes of the forward's row-wise FP8 copy)."""
     from oracle import mxfp4_oracle as Q
     src, R = _rows_of(L, wl)
     xg = _gathered(inp["x"].float().numpy(), src, wl.k, np.arange(R))
     c4, s4 = Q.mxfp4_from_mxfp8(*O.mx_quantize(xg, axis=1))
     np.testing.assert_array_equal(u8(L.part("x4_q_row")).reshape(R, wl.H // 2), Q.pack_e2m1(c4))
-    np.testing.assert_array_equal(
-        scales_tiled_to_rowmajor(u8(L.part("x4_s_row")), R, wl.H), s4)
     c8c, s8c = Q.mxfp8_col_from_mxfp4_row(c4, s4)
     np.testing.assert_array_equal(u8(L.part("x_q_col")).reshape(wl.H, R), c8c)
     np.testing.assert_array_equal(
@@ -215,7 +233,8 @@ def test_act4_layer_full_parity(T, H, F, E, k, zs, ze, of):
     wl = I.Workload("edge_mx4", T, H, F, E, k, "mxfp8", 3100 + T + E, zipf_s=zs,
                     zero_experts=ze, outlier_frac=of)
     inp = I.make_all(wl)
-    L, g = _run(wl, inp, precision="mxfp8_act4")
+    L, g = _run(wl, inp, precision="mxfp8_act4",
+                after_forward=lambda L: _check_act4_x_forward(L, wl, inp))
     x, lg = f64(inp["x"]), f64(inp["logits"])
     w1, w2, dout = f64(inp["w1"]), f64(inp["w2"]), f64(inp["dout"])
     fwd = O.layer_forward(x, lg, w1, w2, wl.k, mx="act4")
