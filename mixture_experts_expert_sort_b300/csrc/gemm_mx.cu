@@ -53,12 +53,9 @@ constexpr int BK = 128;  // bytes of E4M3 = elements per stage
 constexpr int kMaxGroups = gemm::kMaxGroups;
 
 constexpr int kABytes = BM * BK;
-constexpr int kBBytes = BN * BK;
 constexpr int kSfaBytes = 512;
-constexpr int kSfbBytes = 1024;
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kSfbBytes = 1024;  // both 128-row halves of the tile's B scales
 constexpr int kSfStageBytes = kSfaBytes + kSfbBytes;
-constexpr int kTxBytes = kStageBytes + kSfStageBytes;
 // Per-warp transpose buffer of the column-wise quantiser: 32 rows x 36 words
 // (rows 16-byte aligned for vector writes; column reads hit 32 banks).
 constexpr int kXposeStride = 36;
@@ -79,9 +76,20 @@ __host__ __device__ constexpr int round1024(int x) { return (x + 1023) / 1024 * 
 // epilogue warps (two per TMEM lane quarter, each taking every other
 // 32-column chunk) and keep a 3-stage ring to make room for the warps'
 // transpose buffers.
-template <bool FUSED>
+//
+// CG = 2: a CTA pair shares each tile (M = 256 rows, the leader issuing the
+// MMAs): each CTA stages its own 128 rows of A and half of the tile's B rows
+// (32 KB per stage instead of 48), plus the scales of its A rows and of all
+// the tile's B rows (each SM's tensor core reads the scales of every column
+// of B it multiplies from its own tensor memory). The stage bytes freed go to
+// a deeper ring.
+template <bool FUSED, int CG = 1>
 struct Cfg {
-  static constexpr int kStages = FUSED ? 3 : 4;
+  static constexpr int kStages = FUSED ? (CG == 2 ? 4 : 3) : (CG == 2 ? 5 : 4);
+  static constexpr int kBBytes = (BN / CG) * BK;  // this CTA's B rows per stage
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  // bytes of one stage counted on the leader's full barrier (both CTAs of a pair)
+  static constexpr int kTxBytes = CG * (kStageBytes + kSfStageBytes);
   static constexpr int kEpiWarps = FUSED ? 8 : 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   // A/B stages stay 1024-byte aligned (128B-swizzle atoms); the scale tiles
@@ -97,13 +105,14 @@ struct Cfg {
   static constexpr int kSmemBytes = kPrefixOffset + (kMaxGroups + 1) * 4;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;
   static_assert(kSmemAlloc <= 232448, "shared memory budget");
+  static_assert(448 + kStages * 12 <= 512, "TMEM budget: scale columns of every stage");
 };
 
 // Tensor-memory columns.
 constexpr int kAcc1Col = 192;     // accumulator of odd tiles: [192, 448)
 constexpr int kSfTmemCol = 448;   // scale factors: [448, 512)
 constexpr int kSfColsPerStage = 12;  // 4 (A) + 8 (B)
-static_assert(kSfTmemCol + 4 * kSfColsPerStage <= 512, "TMEM budget");
+static_assert(kSfTmemCol + 5 * kSfColsPerStage <= 512, "TMEM budget");
 static_assert(kAcc1Col + BN <= kSfTmemCol, "TMEM budget");
 
 struct MxParams {
@@ -140,9 +149,10 @@ struct TileInfo {
   int k_iters;
 };
 
-template <int MODE>
+template <int MODE, int CG>
 __device__ __forceinline__ void decode_tile(const MxParams& p, const int* prefix, int t,
                                             int& e_hint, TileInfo& ti) {
+  constexpr int kTileM = BM * CG;
   int e = e_hint;
   while (prefix[e + 1] <= t) ++e;
   e_hint = e;
@@ -152,12 +162,12 @@ __device__ __forceinline__ void decode_tile(const MxParams& p, const int* prefix
   ti.row0 = o0;
   ti.rows = (int)(o1 - o0);
   if (MODE == FPROP) {
-    const int mtiles = (ti.rows + BM - 1) / BM;
+    const int mtiles = (ti.rows + kTileM - 1) / kTileM;
     ti.mt = local % mtiles;
     ti.nt = local / mtiles;
     ti.k_iters = p.K / BK;
   } else {
-    const int mtiles = p.M / BM;
+    const int mtiles = p.M / kTileM;
     ti.mt = local % mtiles;
     ti.nt = local / mtiles;
     ti.k_iters = ti.rows / BK;
@@ -461,8 +471,10 @@ __device__ __forceinline__ void epilogue_tile(const MxParams& p, const TileInfo&
                                               const CUtensorMap* tm_gu, const CUtensorMap* tm_qr,
                                               const CUtensorMap* tm_qc, uint32_t gu_bar,
                                               uint32_t& gu_phase, bool& gu_pending,
-                                              volatile int* s_abort) {
-  const long long lrow = (long long)ti.mt * BM + q * 32 + lane;
+                                              volatile int* s_abort, int rbase) {
+  // rbase: first row of this CTA's 128 rows within the group (FPROP) or of M
+  // (WGRAD)
+  const long long lrow = (long long)rbase + q * 32 + lane;
   const bool has_acc = ti.k_iters > 0;
   if (MODE == WGRAD) {
     __nv_bfloat16* crow = p.C + (long long)ti.e * p.c_group_stride + lrow * p.ldc +
@@ -482,7 +494,7 @@ __device__ __forceinline__ void epilogue_tile(const MxParams& p, const TileInfo&
   }
   const bool row_ok = lrow < ti.rows;
   const long long grow = ti.row0 + lrow;
-  const long long rb = ti.row0 + (long long)ti.mt * BM + q * 32;  // first row of the warp
+  const long long rb = ti.row0 + (long long)rbase + q * 32;  // first row of the warp
   if (EPI == EPI_STORE) {
     const int ncol = p.N - ti.nt * BN;
     __nv_bfloat16* crow = p.C + grow * p.ldc + (long long)ti.nt * BN;
@@ -528,14 +540,19 @@ __device__ __forceinline__ void epilogue_tile(const MxParams& p, const TileInfo&
   }
 }
 
-template <int MODE, int EPI>
-__global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
+template <int MODE, int EPI, int CG>
+__global__ void __launch_bounds__(Cfg<EPI != EPI_STORE, CG>::kThreads, 1)
     grouped_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmSFA,
+                             const __grid_constant__ CUtensorMap tmSFB,
                              const __grid_constant__ CUtensorMap tmC,
                              const __grid_constant__ CUtensorMap tmQr,
                              const __grid_constant__ CUtensorMap tmQc, const MxParams p) {
-  using L = Cfg<EPI != EPI_STORE>;
+  using L = Cfg<EPI != EPI_STORE, CG>;
+  constexpr bool kPair = CG == 2;
+  constexpr int kTileM = BM * CG;
+  constexpr int kStageBytes = L::kStageBytes;
   constexpr int kStages = L::kStages;
   constexpr int kSfOffset = L::kSfOffset;
   constexpr int kBarOffset = L::kBarOffset;
@@ -562,6 +579,10 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = (p.N + BN - 1) / BN;
+  // CTA pairs: rank 0 (the leader) issues the MMAs; tiles are dealt out per pair.
+  const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
+  const int unit = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int n_units = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -569,7 +590,9 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
       ptx::mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) ptx::mbar_init(tfull_bar(b), 1);
-    for (int r = 0; r < 3; ++r) ptx::mbar_init(region_bar(r), kEpiThreads);
+    // single CTA: every epilogue thread releases a region; pair: one arrival
+    // per epilogue warp of both CTAs, on the leader's barrier
+    for (int r = 0; r < 3; ++r) ptx::mbar_init(region_bar(r), kPair ? 2 * L::kEpiWarps : kEpiThreads);
     ptx::mbar_init(drain_bar, 1);
     if (EPI != EPI_STORE)
       for (int w = 0; w < L::kEpiWarps; ++w) ptx::mbar_init(gu_bar_of(w), 1);
@@ -581,7 +604,7 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
     for (int e = 0; e < p.E; ++e) {
       int rows = p.offsets[e + 1] - p.offsets[e];
       if (rows % BM) bad = true;
-      int mt = (MODE == FPROP) ? (rows + BM - 1) / BM : p.M / BM;
+      int mt = (MODE == FPROP) ? (rows + kTileM - 1) / kTileM : p.M / kTileM;
       acc += mt * n_tiles;
       s_prefix[e + 1] = acc;
     }
@@ -594,6 +617,8 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
+    ptx::tma_prefetch_desc(&tmSFA);
+    ptx::tma_prefetch_desc(&tmSFB);
     if (EPI != EPI_STORE) {
       ptx::tma_prefetch_desc(&tmC);
       ptx::tma_prefetch_desc(&tmQr);
@@ -601,11 +626,21 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
     }
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(s_tmem), 512);
-    ptx::tmem_relinquish();
+    if (kPair) {
+      ptx::tmem_alloc_cg2(ptx::smem_u32(s_tmem), 512);
+      ptx::tmem_relinquish_cg2();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(s_tmem), 512);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  // A pair's barriers must be initialised in both CTAs before either CTA's
+  // copies, commits or arrivals can reach them.
+  if (kPair)
+    ptx::cluster_sync();
+  else
+    __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
   const int total_tiles = s_prefix[p.E];
@@ -620,11 +655,12 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
       for (int s = 0; s < kStages; ++s) armed[s] = false;
       int e_hint = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      for (int t = unit; t < total_tiles && ok; t += n_units) {
         TileInfo ti;
-        decode_tile<MODE>(p, s_prefix, t, e_hint, ti);
-        const long long a_row = (MODE == FPROP) ? ti.row0 + (long long)ti.mt * BM
-                                                : (long long)ti.mt * BM;
+        decode_tile<MODE, CG>(p, s_prefix, t, e_hint, ti);
+        // this CTA's 128 rows of A
+        const long long a_row = (MODE == FPROP ? ti.row0 : 0LL) + (long long)ti.mt * kTileM +
+                                (long long)rank * BM;
         for (int kb = 0; kb < ti.k_iters; ++kb) {
           if (!gemm::wait_bar(empty_bar(stage), phase ^ 1u, s_abort)) {
             ok = false;
@@ -634,13 +670,23 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
           const uint32_t b_dst = a_dst + kABytes;
           const uint32_t sfa_dst = sbase + kSfOffset + stage * kSfStageBytes;
           const uint32_t sfb_dst = sfa_dst + kSfaBytes;
-          ptx::mbar_arrive_expect_tx(full_bar(stage), kTxBytes);
-          armed[stage] = true;
-          armed_phase[stage] = phase;
+          // Completion of both CTAs' copies of a pair is counted on the leader's barrier.
+          const uint32_t fb = kPair ? ptx::mapa_shared(full_bar(stage), 0) : full_bar(stage);
+          if (rank == 0) {
+            ptx::mbar_arrive_expect_tx(full_bar(stage), L::kTxBytes);
+            armed[stage] = true;
+            armed_phase[stage] = phase;
+          }
+          auto load = [&](uint32_t dst, const CUtensorMap* tm, long long c0, long long c1) {
+            if (kPair)
+              ptx::tma_load_2d_cg2(dst, tm, (int)c0, (int)c1, fb);
+            else
+              ptx::tma_load_2d(dst, tm, (int)c0, (int)c1, fb);
+          };
           const long long a_k = (MODE == FPROP) ? (long long)kb * BK : ti.row0 + (long long)kb * BK;
-          ptx::tma_load_2d(a_dst, &tmA, (int)a_k, (int)a_row, full_bar(stage));
-          ptx::bulk_load(sfa_dst, p.sfa + ((a_row / 128) * p.sfa_ktiles + a_k / 128) * 512,
-                         kSfaBytes, full_bar(stage));
+          load(a_dst, &tmA, a_k, a_row);
+          // a 512-byte scale tile is one row of 128 words of the scale map
+          load(sfa_dst, &tmSFA, (a_k / 128) * 128, a_row / 128);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             long long b_row, b_k;
@@ -651,14 +697,12 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
               b_row = (long long)ti.nt * BN + h * (BN / 2);
               b_k = a_k;
             }
-            ptx::tma_load_2d(b_dst + h * (BN / 2) * BK, &tmB, (int)b_k, (int)b_row,
-                             full_bar(stage));
-            // A half past the last row of B (the N tail of the last expert) reads
-            // zeros through TMA; its scales are never used, so fetch the last tile.
-            const long long sb_row = b_row < p.b_rows ? b_row : p.b_rows - 128;
-            ptx::bulk_load(sfb_dst + h * 512,
-                           p.sfb + ((sb_row / 128) * p.sfb_ktiles + b_k / 128) * 512, 512,
-                           full_bar(stage));
+            // B rows: both halves (one CTA), or this CTA's half (pair). A half
+            // past the last row of B (the N tail of the last expert) reads
+            // zeros, data and scales alike.
+            if (!kPair || h == (int)rank) load(b_dst + (kPair ? 0 : h * (BN / 2) * BK), &tmB, b_k, b_row);
+            // B scales: both halves in every CTA
+            load(sfb_dst + h * 512, &tmSFB, (b_k / 128) * 128, b_row / 128);
           }
           if (++stage == kStages) {
             stage = 0;
@@ -671,16 +715,17 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
-    if (ptx::elect_one()) {
+    if (rank == 0 && ptx::elect_one()) {
+      constexpr uint16_t kBoth = 3;  // commit to the barrier of both CTAs of a pair
       int stage = 0;
       uint32_t phase = 0;
       int e_hint = 0;
       bool ok = true;
       uint32_t uses[3] = {0, 0, 0};  // completed uses of each TMEM region
       int j = 0;                      // tiles processed by this CTA
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++j) {
+      for (int t = unit; t < total_tiles && ok; t += n_units, ++j) {
         TileInfo ti;
-        decode_tile<MODE>(p, s_prefix, t, e_hint, ti);
+        decode_tile<MODE, CG>(p, s_prefix, t, e_hint, ti);
         const int own = (j & 1) ? 2 : 0;
         // Wait until both regions of this tile were drained by the epilogue.
         if (!gemm::wait_bar(region_bar(1), (uses[1] & 1u) ^ 1u, s_abort)) break;
@@ -701,33 +746,52 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
           const uint32_t sfb_addr = sfa_addr + kSfaBytes;
           const uint32_t sf_col = kSfTmemCol + stage * kSfColsPerStage;
           // scales: smem (32 rows x 16 B per 128-row tile) -> TMEM, 4 columns each
-          ptx::tmem_cp_32x128b_warpx4(tmem_base + sf_col,
-                                      ptx::smem_desc(sfa_addr, 128, 128, ptx::kSwizzleNone));
-          ptx::tmem_cp_32x128b_warpx4(tmem_base + sf_col + 4,
-                                      ptx::smem_desc(sfb_addr, 128, 128, ptx::kSwizzleNone));
-          ptx::tmem_cp_32x128b_warpx4(tmem_base + sf_col + 8,
-                                      ptx::smem_desc(sfb_addr + 512, 128, 128,
-                                                     ptx::kSwizzleNone));
+          // (in each CTA of a pair, from its own shared memory)
+          const uint64_t sd[3] = {ptx::smem_desc(sfa_addr, 128, 128, ptx::kSwizzleNone),
+                                  ptx::smem_desc(sfb_addr, 128, 128, ptx::kSwizzleNone),
+                                  ptx::smem_desc(sfb_addr + 512, 128, 128, ptx::kSwizzleNone)};
+#pragma unroll
+          for (int c = 0; c < 3; ++c) {
+            if (kPair)
+              ptx::tmem_cp_32x128b_warpx4_cg2(tmem_base + sf_col + 4 * c, sd[c]);
+            else
+              ptx::tmem_cp_32x128b_warpx4(tmem_base + sf_col + 4 * c, sd[c]);
+          }
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t da = ptx::smem_desc(a_addr + kk * 32, 16, 1024, ptx::kSwizzle128B);
             const uint64_t db = ptx::smem_desc(b_addr + kk * 32, 16, 1024, ptx::kSwizzle128B);
-            ptx::mma_mxf8(d_tmem, da, db, ptx::idesc_mxf8(BM, BN, kk, kk), tmem_base + sf_col,
-                          tmem_base + sf_col + 4, (kb | kk) ? 1u : 0u);
+            if (kPair)
+              ptx::mma_mxf8_cg2(d_tmem, da, db, ptx::idesc_mxf8(kTileM, BN, kk, kk),
+                                tmem_base + sf_col, tmem_base + sf_col + 4, (kb | kk) ? 1u : 0u);
+            else
+              ptx::mma_mxf8(d_tmem, da, db, ptx::idesc_mxf8(BM, BN, kk, kk), tmem_base + sf_col,
+                            tmem_base + sf_col + 4, (kb | kk) ? 1u : 0u);
           }
-          ptx::mma_commit(empty_bar(stage));
+          if (kPair)
+            ptx::mma_commit_cg2(empty_bar(stage), kBoth);
+          else
+            ptx::mma_commit(empty_bar(stage));
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        if (ti.k_iters > 0)
-          ptx::mma_commit(tfull_bar(j & 1));
-        else
+        if (ti.k_iters > 0) {
+          if (kPair)
+            ptx::mma_commit_cg2(tfull_bar(j & 1), kBoth);
+          else
+            ptx::mma_commit(tfull_bar(j & 1));
+        } else {
           ptx::mbar_arrive(tfull_bar(j & 1));
+          if (kPair) ptx::mbar_arrive_remote(ptx::mapa_shared(tfull_bar(j & 1), 1));
+        }
       }
-      ptx::mma_commit(drain_bar);
+      if (kPair)
+        ptx::mma_commit_cg2(drain_bar, 1);
+      else
+        ptx::mma_commit(drain_bar);
       gemm::drain_wait(drain_bar, 0);
     }
   } else {
@@ -743,10 +807,31 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
     const uint32_t tl_lanes = tmem_base + ((uint32_t)(q * 32) << 16);
     int e_hint = 0;
     int j = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++j) {
+    // Release of a TMEM region: every thread (one CTA), or one arrival per warp
+    // on the leader's barrier (pair).
+    auto release = [&](int r) {
+      ptx::tc_fence_before();
+      if (kPair) {
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0)
+            ptx::mbar_arrive(region_bar(r));
+          else
+            ptx::mbar_arrive_remote(ptx::mapa_shared(region_bar(r), 0));
+        }
+      } else {
+        ptx::mbar_arrive(region_bar(r));
+      }
+    };
+    for (int t = unit; t < total_tiles; t += n_units, ++j) {
       TileInfo ti;
-      decode_tile<MODE>(p, s_prefix, t, e_hint, ti);
-      if (EPI == EPI_SWIGLU_BWD) {
+      decode_tile<MODE, CG>(p, s_prefix, t, e_hint, ti);
+      // This CTA's rows of the tile; in a pair the second CTA's half of the
+      // last tile of a group can lie past the group (groups are padded to 128
+      // rows): its accumulator is then not stored.
+      const int rbase = ti.mt * kTileM + (int)rank * BM;
+      const bool live = MODE == WGRAD || rbase < ti.rows;
+      if (EPI == EPI_SWIGLU_BWD && live) {
         // The saved gate/up of this warp's first chunk does not depend on the
         // accumulator: fetch it while the tile's MMAs run.
         const uint32_t ord = bwd_chunk_order((j & 1) != 0, h, p.N - ti.nt * BN);
@@ -754,7 +839,7 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
           if (lane == 0) {
             ptx::fence_proxy_async_smem();  // after the previous tile's reads of the boxes
             load_gu(&tmC, ptx::smem_u32(gu_stage), bwd_col(ti, (int)(ord & 15)), p.F,
-                    (int)(ti.row0 + (long long)ti.mt * BM + q * 32), gu_bar);
+                    (int)(ti.row0 + (long long)rbase + q * 32), gu_bar);
           }
           gu_pending = true;
         }
@@ -766,7 +851,7 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
       // 192 + 32h for the fused kernels, all 64 for the plain ones) and hand
       // the region back to the MMA thread.
       float sh[32 * NSH];
-      if (ti.k_iters > 0) {
+      if (ti.k_iters > 0 && live) {
 #pragma unroll
         for (int c = 0; c < NSH; ++c) {
           uint32_t v[32];
@@ -779,13 +864,12 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32 * NSH; ++i) sh[i] = 0.f;
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(region_bar(1));
-      epilogue_tile<MODE, EPI>(p, ti, odd, h, sh, tl_lanes + (odd ? (uint32_t)kAcc1Col : 0u), q,
-                               lane, xs, gu_stage, &tmC, &tmQr, &tmQc, gu_bar, gu_phase,
-                               gu_pending, s_abort);
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(region_bar(odd ? 2 : 0));
+      release(1);
+      if (live)
+        epilogue_tile<MODE, EPI>(p, ti, odd, h, sh, tl_lanes + (odd ? (uint32_t)kAcc1Col : 0u),
+                                 q, lane, xs, gu_stage, &tmC, &tmQr, &tmQc, gu_bar, gu_phase,
+                                 gu_pending, s_abort, rbase);
+      release(odd ? 2 : 0);
     }
     // Bulk stores must be complete, and a gate/up load left in flight by an
     // abort must have landed, before this CTA's shared memory goes away.
@@ -795,30 +879,88 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE>::kThreads, 1)
     }
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  // A pair leaves together: the leader's MMAs write the peer's tensor memory
+  // and the peer's copies and arrivals reach the leader's barriers.
+  if (kPair)
+    ptx::cluster_sync();
+  else
+    __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, 512);
+    if (kPair)
+      ptx::tmem_dealloc_cg2(tmem_base, 512);
+    else
+      ptx::tmem_dealloc(tmem_base, 512);
   }
 }
 
-template <int MODE, int EPI>
-static int launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-                  const CUtensorMap& tqr, const CUtensorMap& tqc, const MxParams& p,
-                  long long tiles_bound, cudaStream_t st) {
-  using L = Cfg<EPI != EPI_STORE>;
-  auto kern = grouped_gemm_mxf8_kernel<MODE, EPI>;
+// Tensor maps of one launch: A and B data, their scale tiles, and the fused
+// epilogues' gate/up and code maps (the plain kernels pass any map there).
+struct Maps {
+  CUtensorMap a, b, sfa, sfb, c, qr, qc;
+};
+
+// tiles_bound: an upper bound on the launch's 128-row tiles.
+template <int MODE, int EPI, int CG = 1>
+static int launch(const Maps& m, const MxParams& p, long long tiles_bound, cudaStream_t st) {
+  using L = Cfg<EPI != EPI_STORE, CG>;
+  auto kern = grouped_gemm_mxf8_kernel<MODE, EPI, CG>;
   static bool attr_set = false;
+  static int max_units = 0;  // co-resident CTAs (CG = 1) or CTA pairs (CG = 2)
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
+    max_units = gemm::num_sms();
+    if (CG == 2) {
+      cudaLaunchConfig_t q = {};
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = 2;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      q.gridDim = dim3(2 * (gemm::num_sms() / 2));
+      q.blockDim = dim3(L::kThreads);
+      q.dynamicSmemBytes = L::kSmemAlloc;
+      q.attrs = qa;
+      q.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n < 1) return MOE_ERR_CUDA;
+      max_units = n;
+    }
     attr_set = true;
   }
-  long long grid = tiles_bound < gemm::num_sms() ? tiles_bound : gemm::num_sms();
-  if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, L::kThreads, L::kSmemAlloc, st>>>(ta, tb, tc, tqr, tqc, p);
+  long long units = tiles_bound < max_units ? tiles_bound : max_units;
+  if (units < 1) units = 1;
+  if (CG == 1) {
+    kern<<<(unsigned)units, L::kThreads, L::kSmemAlloc, st>>>(m.a, m.b, m.sfa, m.sfb, m.c, m.qr,
+                                                              m.qc, p);
+    return launch_status();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(2 * units));
+  cfg.blockDim = dim3(L::kThreads);
+  cfg.dynamicSmemBytes = L::kSmemAlloc;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, m.a, m.b, m.sfa, m.sfb, m.c, m.qr, m.qc, p) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return launch_status();
+}
+
+// The tiled scales of an MXFP8 operand with mn rows and kdim columns as a 2-D
+// tensor of 512-byte tiles: one row of (kdim/128) * 128 words per 128 rows of
+// the operand, loaded a tile (128 words) at a time.
+static bool scale_map(CUtensorMap* m, const void* base, long long mn, long long kdim) {
+  return gemm::make_tmap(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, mn / 128, (kdim / 128) * 128,
+                         (kdim / 128) * 128, 1, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 static bool u8_map(CUtensorMap* m, const void* base, long long rows, long long cols) {
@@ -885,18 +1027,22 @@ extern "C" int moe_grouped_gemm_mxfp8(int mode, const uint8_t* a, const uint8_t*
   p.b_rows = b_rows;
   p.C = static_cast<__nv_bfloat16*>(C);
   p.ldc = N;
-  CUtensorMap ta, tb;
-  if (!MX::u8_map(&ta, a, a_rows, a_cols) || !MX::u8_map(&tb, b, b_rows, b_cols)) return MOE_ERR_CUDA;
+  MX::Maps m;
+  if (!MX::u8_map(&m.a, a, a_rows, a_cols) || !MX::u8_map(&m.b, b, b_rows, b_cols) ||
+      !MX::scale_map(&m.sfa, sa, a_rows, a_cols) || !MX::scale_map(&m.sfb, sb, b_rows, b_cols))
+    return MOE_ERR_CUDA;
+  m.c = m.qr = m.qc = m.b;  // not used by the plain epilogue
   cudaStream_t st = (cudaStream_t)stream;
   if (mode == MOE_GEMM_FPROP) {
     p.b_row_stride = b_row_stride;
     p.b_k_stride = b_k_stride;
     long long bound = (a_rows / MX::BM + E) * (long long)((N + MX::BN - 1) / MX::BN);
-    return MX::launch<FPROP, EPI_STORE>(ta, tb, tb, tb, tb, p, bound, st);
+    return MX::launch<FPROP, EPI_STORE, 2>(m, p, bound, st);
   }
   p.c_group_stride = (long long)M * N;
   long long bound = (long long)E * (M / MX::BM) * (N / MX::BN);
-  return MX::launch<WGRAD, EPI_STORE>(ta, tb, tb, tb, tb, p, bound, st);
+  if (M % 256 == 0) return MX::launch<WGRAD, EPI_STORE, 2>(m, p, bound, st);
+  return MX::launch<WGRAD, EPI_STORE>(m, p, bound, st);
 }
 
 extern "C" int moe_fc1_swiglu_mxfp8(const uint8_t* xq, const uint8_t* sx, long long rows, int H,
@@ -932,20 +1078,22 @@ extern "C" int moe_fc1_swiglu_mxfp8(const uint8_t* xq, const uint8_t* sx, long l
   p.q_col = hq_col;
   p.s_col = sh_col;
   p.q_col_ld = rows;
-  CUtensorMap ta, tb, tc, tqr, tqc;
-  if (!MX::u8_map(&ta, xq, rows, H) || !MX::u8_map(&tb, w1t, 2LL * F, (long long)E * H))
+  MX::Maps m;
+  if (!MX::u8_map(&m.a, xq, rows, H) || !MX::u8_map(&m.b, w1t, 2LL * F, (long long)E * H) ||
+      !MX::scale_map(&m.sfa, sx, rows, H) ||
+      !MX::scale_map(&m.sfb, sw1t, 2LL * F, (long long)E * H))
     return MOE_ERR_CUDA;
   // [g | u] output, written by TMA in 32 x 32 boxes
-  if (!gemm::make_tmap(&tc, gu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, 2LL * F, 2LL * F, 32,
+  if (!gemm::make_tmap(&m.c, gu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, 2LL * F, 2LL * F, 32,
                        32, CU_TENSOR_MAP_SWIZZLE_NONE))
     return MOE_ERR_CUDA;
   // H codes: row-wise [rows, F], column-wise [F, rows] (the row-wise map
   // stands in when there is no column-wise copy; it is then never used)
-  if (!MX::code_map(&tqr, hq_row, rows, F) ||
-      !MX::code_map(&tqc, hq_col ? hq_col : hq_row, hq_col ? F : rows, hq_col ? rows : F))
+  if (!MX::code_map(&m.qr, hq_row, rows, F) ||
+      !MX::code_map(&m.qc, hq_col ? hq_col : hq_row, hq_col ? F : rows, hq_col ? rows : F))
     return MOE_ERR_CUDA;
   long long bound = (rows / MX::BM + E) * (long long)(F / 128);
-  return MX::launch<FPROP, EPI_SWIGLU_FWD>(ta, tb, tc, tqr, tqc, p, bound, (cudaStream_t)stream);
+  return MX::launch<FPROP, EPI_SWIGLU_FWD, 2>(m, p, bound, (cudaStream_t)stream);
 }
 
 extern "C" int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t* sdy2,
@@ -984,15 +1132,18 @@ extern "C" int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t
   p.q_col_ld = rows;
   p.dp_part = dp_part;
   p.n_part = 2 * ((F + MX::BN - 1) / MX::BN);  // two epilogue warps per row and tile
-  CUtensorMap ta, tb, tgu, tqr, tqc;
-  if (!MX::u8_map(&ta, dy2q, rows, H) || !MX::u8_map(&tb, w2q, (long long)E * F, H)) return MOE_ERR_CUDA;
+  MX::Maps m;
+  if (!MX::u8_map(&m.a, dy2q, rows, H) || !MX::u8_map(&m.b, w2q, (long long)E * F, H) ||
+      !MX::scale_map(&m.sfa, sdy2, rows, H) || !MX::scale_map(&m.sfb, sw2, (long long)E * F, H))
+    return MOE_ERR_CUDA;
   // saved [g | u], read by TMA in 32 x 32 boxes with the 64-byte swizzle
-  if (!gemm::make_tmap(&tgu, gu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, 2LL * F, 2LL * F, 32,
+  if (!gemm::make_tmap(&m.c, gu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, 2LL * F, 2LL * F, 32,
                        32, CU_TENSOR_MAP_SWIZZLE_64B))
     return MOE_ERR_CUDA;
   // dY1 codes: row-wise [rows, 2F], column-wise [2F, rows]
-  if (!MX::code_map(&tqr, dy1q_row, rows, 2LL * F) || !MX::code_map(&tqc, dy1q_col, 2LL * F, rows))
+  if (!MX::code_map(&m.qr, dy1q_row, rows, 2LL * F) ||
+      !MX::code_map(&m.qc, dy1q_col, 2LL * F, rows))
     return MOE_ERR_CUDA;
   long long bound = (rows / MX::BM + E) * (long long)((F + MX::BN - 1) / MX::BN);
-  return MX::launch<FPROP, EPI_SWIGLU_BWD>(ta, tb, tgu, tqr, tqc, p, bound, (cudaStream_t)stream);
+  return MX::launch<FPROP, EPI_SWIGLU_BWD, 2>(m, p, bound, (cudaStream_t)stream);
 }

@@ -330,6 +330,29 @@ __device__ __forceinline__ void mma_bf16_cg2(uint32_t d_tmem, uint64_t a_desc, u
       : "memory");
 }
 
+// Block-scaled MXFP8 MMA for a CTA pair: each CTA's tensor core takes the
+// scale factors of its own rows of A and of all N columns of B from its own
+// tensor memory, at the same addresses.
+__device__ __forceinline__ void mma_mxf8_cg2(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Shared memory -> tensor memory copy (32 rows x 128 bits, replicated to the
+// four lane quarters) in each CTA of the pair, from that CTA's own shared
+// memory at sdesc to its own tensor memory at taddr; issued by the leader.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4_cg2(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
 // Arrive on the mbarrier at offset `bar` in every CTA of `cta_mask` when the
 // CTA pair's tcgen05 operations issued so far by this thread have completed.
 __device__ __forceinline__ void mma_commit_cg2(uint32_t bar, uint16_t cta_mask) {
