@@ -271,19 +271,17 @@ __device__ __forceinline__ void load_gu(const CUtensorMap* tm_gu, uint32_t dst, 
 
 // Accumulator chunk c (tile-local, 32 columns) of this warp's 32 rows: a copy
 // of `regs` when given (the chunk drained from the shared TMEM region), else
-// read from TMEM.
-__device__ __forceinline__ void load_acc(int c, const float* regs, uint32_t tl_tile, float* f) {
+// read from TMEM. The read is only issued here; acc_ready() waits for it, so
+// work that does not need the values can go in between.
+__device__ __forceinline__ void load_acc(int c, const float* regs, uint32_t tl_tile, uint32_t* v) {
   if (regs) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) f[i] = regs[i];
+    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(regs[i]);
   } else {
-    uint32_t v[32];
     ptx::tmem_ld_32x32b_x32(tl_tile + c * 32, v);
-    ptx::tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
   }
 }
+__device__ __forceinline__ void acc_ready() { ptx::tmem_ld_wait(); }
 
 // Element i (a compile-time index after unrolling) of 32 packed bf16 values.
 __device__ __forceinline__ float bf16_at(const uint4* s, int i) {
@@ -318,15 +316,22 @@ __device__ __forceinline__ void fwd_pair(const MxParams& p, const TileInfo& ti, 
                                          const CUtensorMap* tm_qr, const CUtensorMap* tm_qc) {
   const long long F = p.F;
   uint8_t* xb = reinterpret_cast<uint8_t*>(xs);
-  float g[32], u[32];
-  load_acc(c, g_regs, tl_tile, g);
-  load_acc(c + 4, u_regs, tl_tile, u);
+  uint32_t gv[32], uv[32];
+  load_acc(c, g_regs, tl_tile, gv);
+  load_acc(c + 4, u_regs, tl_tile, uv);
   const long long col = (long long)ti.nt * (BN / 2) + c * 32;
   // [g | u] in bf16: the warp's 32 x 32 gate and up boxes are staged in shared
   // memory (row `lane` = 64 bytes each) and written by TMA. The wait also
   // frees this warp's code boxes of its previous chunk.
   if (lane == 0) ptx::bulk_wait_read_all();
   __syncwarp();
+  acc_ready();
+  float g[32], u[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    g[i] = __uint_as_float(gv[i]);
+    u[i] = __uint_as_float(uv[i]);
+  }
   gemm::store32_bf16(reinterpret_cast<__nv_bfloat16*>(gu_stage + lane * 64), g);
   gemm::store32_bf16(reinterpret_cast<__nv_bfloat16*>(gu_stage + 2048 + lane * 64), u);
   ptx::fence_proxy_async_smem();
@@ -395,8 +400,9 @@ __device__ __forceinline__ bool bwd_chunk(const MxParams& p, const TileInfo& ti,
   const int c = (int)((ord >> (4 * i)) & 15);
   const long long col = bwd_col(ti, c);
   uint8_t* xb = reinterpret_cast<uint8_t*>(xs);
-  float dg[32], du[32];
-  load_acc(c, regs, tl_tile, dg);  // dH for now
+  uint32_t dhv[32];
+  load_acc(c, regs, tl_tile, dhv);  // dH (awaited here: holding it across the gate/up wait spills)
+  acc_ready();
   if (!gemm::wait_bar(gu_bar, gu_phase, s_abort)) return false;
   gu_phase ^= 1u;
   gu_pending = false;
@@ -420,6 +426,9 @@ __device__ __forceinline__ bool bwd_chunk(const MxParams& p, const TileInfo& ti,
     }
     gu_pending = true;
   }
+  float dg[32], du[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) dg[j] = __uint_as_float(dhv[j]);  // dH for now
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     const float g = bf16_at(gc, j), u = bf16_at(uc, j);
@@ -1145,5 +1154,7 @@ extern "C" int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t
       !MX::code_map(&m.qc, dy1q_col, 2LL * F, rows))
     return MOE_ERR_CUDA;
   long long bound = (rows / MX::BM + E) * (long long)((F + MX::BN - 1) / MX::BN);
-  return MX::launch<FPROP, EPI_SWIGLU_BWD, 2>(m, p, bound, (cudaStream_t)stream);
+  // The SwiGLU-backward epilogue, not the MMA, bounds this kernel: a CTA pair
+  // measured slightly slower than one CTA per tile.
+  return MX::launch<FPROP, EPI_SWIGLU_BWD, 1>(m, p, bound, (cudaStream_t)stream);
 }
