@@ -69,15 +69,21 @@ struct Params {
 
 // CG = 2: a CTA pair shares each tile (M = 256), each CTA staging its own 128
 // rows of A and half of the B columns, so a stage is 32 KB instead of 48.
-template <int BN, int CG = 1>
+// FUSED: the SwiGLU epilogues move their bf16 tiles by TMA through a per-warp
+// buffer (32 x 32 boxes, 2 KB each: FC1 stages g, u and h; the FC2 dgrad
+// receives gate and up and stages dg and du).
+constexpr int kEpiBufBytes = 8192;
+
+template <int BN, int CG = 1, bool FUSED = false>
 struct Smem {
   static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = (BN / CG) * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (CG == 2 || BN != 256) ? 6 : 4;
-  static constexpr int kBarOffset = kStages * kStageBytes;
-  // full[S], empty[S], tfull[2], tempty[2], drain
-  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kEpiOffset = kStages * kStageBytes;  // 1024-byte aligned
+  static constexpr int kBarOffset = kEpiOffset + (FUSED ? 4 * kEpiBufBytes : 0);
+  // full[S], empty[S], tfull[2], tempty[2], drain, gate/up loads[4]
+  static constexpr int kNumBars = 2 * kStages + 5 + (FUSED ? 4 : 0);
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
   // misc: tmem base (4), abort flag (4), tile prefix [kMaxGroups + 1] ints
   static constexpr int kPrefixOffset = kMiscOffset + 16;
@@ -191,11 +197,56 @@ __device__ __forceinline__ float sigmoidf_fast(float z) {
   return r;
 }
 
+// Lane `lane`'s 32 values as bf16 into row `lane` of a 32 x 32 box (64-byte
+// rows) at `box`, in the 64-byte swizzle of a TMA copy with
+// CU_TENSOR_MAP_SWIZZLE_64B: 16-byte chunk i of row r sits at i ^ ((r >> 1) & 3).
+__device__ __forceinline__ void stage_bf16_row(uint8_t* box, int lane, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(box + lane * 64);
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    d[q ^ sw] = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                           pack_bf16(v[8 * q + 4], v[8 * q + 5]),
+                           pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+}
+
+// Row `lane` of such a box as 32 floats.
+__device__ __forceinline__ void read_bf16_row(const uint8_t* box, int lane, float* v) {
+  const uint4* s = reinterpret_cast<const uint4*>(box + lane * 64);
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 u = s[q ^ sw];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * q + 2 * j] = bf16_lo(w[j]);
+      v[8 * q + 2 * j + 1] = bf16_hi(w[j]);
+    }
+  }
+}
+
+// TMA load of the saved gate and up boxes (32 rows x 32 columns, 64-byte
+// swizzle) of gate/up column `col` and row `rb` to dst, completing on bar.
+__device__ __forceinline__ void load_gate_up(const CUtensorMap* tm, uint32_t dst, int col, int F,
+                                             int rb, uint32_t bar) {
+  ptx::mbar_arrive_expect_tx(bar, 4096);
+  ptx::tma_load_2d(dst, tm, col, rb, bar);
+  ptx::tma_load_2d(dst + 2048, tm, F + col, rb, bar);
+}
+
+// tmC, tmD: the fused epilogues' bf16 tiles, written (or read) as 32 x 32
+// boxes by TMA: FC1 + SwiGLU stores [g | u] (tmC) and H (tmD); FC2 dgrad +
+// SwiGLU backward reads the saved [g | u] (tmC) and stores dY1 (tmD). A warp
+// whose 32 rows straddle the end of a group uses per-lane loads and stores.
 template <int MODE, int EPI, int BN, int A_MN, int B_MN, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
-                             const __grid_constant__ CUtensorMap tmB, const Params p) {
-  using L = Smem<BN, CG>;
+                             const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmC,
+                             const __grid_constant__ CUtensorMap tmD, const Params p) {
+  constexpr bool kFused = EPI != EPI_STORE;
+  using L = Smem<BN, CG, kFused>;
   constexpr bool kPair = CG == 2;
   // Rows of A (and columns of B) this CTA stages per stage, and the tile's M.
   constexpr int kTileM = BM * CG;
@@ -210,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * L::kStages + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * L::kStages + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * L::kStages + 4);
+  auto gu_bar_of = [&](int w) { return bar0 + 8u * (2 * L::kStages + 5 + w); };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L::kMiscOffset);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::kMiscOffset + 4);
   int* s_prefix = reinterpret_cast<int*>(smem + L::kPrefixOffset);
@@ -233,6 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(tempty_bar(b), kPair ? 8 : 128);
     }
     ptx::mbar_init(drain_bar, 1);
+    if (kFused)
+      for (int w = 0; w < 4; ++w) ptx::mbar_init(gu_bar_of(w), 1);
     ptx::fence_mbar_init();
     *s_abort = 0;
     // Tile prefix over groups.
@@ -256,6 +310,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
+    if (kFused) {
+      ptx::tma_prefetch_desc(&tmC);
+      ptx::tma_prefetch_desc(&tmD);
+    }
   }
   if (warp == 1) {
     if (kPair) {
@@ -433,9 +491,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int e_hint = 0;
+    uint8_t* ebuf = smem + L::kEpiOffset + (warp - 2) * kEpiBufBytes;  // fused: this warp's boxes
+    const uint32_t ebuf_s = ptx::smem_u32(ebuf);
+    const uint32_t gu_bar = gu_bar_of(warp - 2);
+    uint32_t gu_phase = 0;
+    bool gu_pending = false;  // a gate/up load of this warp is in flight
     for (int t = unit; t < total_tiles; t += n_units) {
       TileInfo ti;
       decode_tile<MODE, BN, CG>(p, s_prefix, t, e_hint, ti);
+      // First row of this warp's 32 within the group, and whether the group
+      // holds all 32 (TMA boxes) or none of them.
+      const int wrow0 = ti.mt * kTileM + (int)rank * BM + q * 32;
+      const bool warp_full = wrow0 + 32 <= ti.rows;
+      const long long rb = ti.row0 + wrow0;
+      if (EPI == EPI_SWIGLU_BWD && MODE == FPROP && warp_full) {
+        // The saved gate/up of the first chunk does not depend on the
+        // accumulator: fetch it while the tile's MMAs run.
+        if (lane == 0) {
+          ptx::fence_proxy_async_smem();  // after the previous tile's reads of the boxes
+          load_gate_up(&tmC, ebuf_s, ti.nt * BN, p.F, (int)rb, gu_bar);
+        }
+        gu_pending = true;
+      }
       if (!wait_bar(tfull_bar(acc), acc_phase, s_abort)) break;
       ptx::tc_fence_after();
       const uint32_t tm = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
@@ -475,6 +552,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
             if (row_ok) store32_bf16(crow + c * 32, f);
           }
+        } else if (EPI == EPI_SWIGLU_FWD && warp_full) {
+          // [g | u] and H leave as 32 x 32 boxes through this warp's buffer
+          const float pr = p.p_rows[grow];
+          const int n0 = ti.nt * (BN / 2);
+          const long long F = p.F;
+#pragma unroll 1
+          for (int c = 0; c < BN / 64; ++c) {
+            uint32_t vg[32], vu[32];
+            ptx::tmem_ld_32x32b_x32(tm + c * 32, vg);
+            ptx::tmem_ld_32x32b_x32(tm + BN / 2 + c * 32, vu);
+            if (lane == 0) ptx::bulk_wait_read_all();  // the previous boxes were read
+            __syncwarp();
+            ptx::tmem_ld_wait();
+            float g[32], u[32], h[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              g[i] = __uint_as_float(vg[i]);
+              u[i] = __uint_as_float(vu[i]);
+              h[i] = g[i] * sigmoidf_fast(g[i]) * u[i] * pr;
+            }
+            stage_bf16_row(ebuf, lane, g);
+            stage_bf16_row(ebuf + 2048, lane, u);
+            stage_bf16_row(ebuf + 4096, lane, h);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int col = n0 + c * 32;
+              ptx::tma_store_2d(&tmC, col, (int)rb, ebuf_s);
+              ptx::tma_store_2d(&tmC, (int)(F + col), (int)rb, ebuf_s + 2048);
+              ptx::tma_store_2d(&tmD, col, (int)rb, ebuf_s + 4096);
+              ptx::bulk_commit_group();
+            }
+          }
         } else if (EPI == EPI_SWIGLU_FWD) {
           const float pr = row_ok ? p.p_rows[grow] : 0.f;
           const int n0 = ti.nt * (BN / 2);
@@ -499,7 +609,59 @@ __global__ void __launch_bounds__(kThreads, 1)
               store32_bf16(p.Hout + grow * F + col, h);
             }
           }
-        } else {  // EPI_SWIGLU_BWD: accumulator holds dH for F-columns [nt*BN, +BN)
+        } else if (warp_full) {  // EPI_SWIGLU_BWD through TMA boxes
+          const float pr = p.p_rows[grow];
+          const int n0 = ti.nt * BN;
+          const long long F = p.F;
+          float dp = 0.f;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(tm + c * 32, v);  // dH, read while gate/up are waited for
+            if (!wait_bar(gu_bar, gu_phase, s_abort)) {
+              ptx::tmem_ld_wait();
+              break;
+            }
+            gu_phase ^= 1u;
+            gu_pending = false;
+            float g[32], u[32];
+            read_bf16_row(ebuf, lane, g);
+            read_bf16_row(ebuf + 2048, lane, u);
+            __syncwarp();  // the warp is done reading the boxes
+            if (c + 1 < BN / 32) {
+              if (lane == 0) {
+                ptx::fence_proxy_async_smem();
+                load_gate_up(&tmC, ebuf_s, n0 + (c + 1) * 32, (int)F, (int)rb, gu_bar);
+              }
+              gu_pending = true;
+            }
+            ptx::tmem_ld_wait();
+            float dg[32], du[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float dh = __uint_as_float(v[i]);
+              const float s = sigmoidf_fast(g[i]);
+              const float silu = g[i] * s;
+              dp = fmaf(dh, silu * u[i], dp);
+              const float da = dh * pr;
+              dg[i] = da * u[i] * s * (1.f + g[i] * (1.f - s));
+              du[i] = da * silu;
+            }
+            if (lane == 0) ptx::bulk_wait_read_all();  // the previous dY1 boxes were read
+            __syncwarp();
+            stage_bf16_row(ebuf + 4096, lane, dg);
+            stage_bf16_row(ebuf + 6144, lane, du);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int col = n0 + c * 32;
+              ptx::tma_store_2d(&tmD, col, (int)rb, ebuf_s + 4096);
+              ptx::tma_store_2d(&tmD, (int)(F + col), (int)rb, ebuf_s + 6144);
+              ptx::bulk_commit_group();
+            }
+          }
+          p.dp_part[grow * p.n_part + ti.nt] = dp;
+        } else {  // EPI_SWIGLU_BWD, per lane: accumulator holds dH for F-columns [nt*BN, +BN)
           const float pr = row_ok ? p.p_rows[grow] : 0.f;
           const int n0 = ti.nt * BN;
           const long long F = p.F;
@@ -548,6 +710,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    // Bulk stores must be complete, and a gate/up load left in flight by an
+    // abort must have landed, before this CTA's shared memory goes away.
+    if (kFused && lane == 0) {
+      ptx::bulk_wait_all();
+      if (gu_pending) drain_wait(gu_bar, gu_phase);
+    }
   }
   ptx::tc_fence_before();
   __syncwarp();
@@ -588,9 +756,12 @@ static int num_sms() {
 // 256-row tiles that CTA pairs take).
 template <int MODE, int EPI, int BN, int A_MN, int B_MN, int CG = 1>
 static int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
-                  long long tiles_bound, cudaStream_t st) {
+                  long long tiles_bound, cudaStream_t st, const CUtensorMap* tc = nullptr,
+                  const CUtensorMap* td = nullptr) {
   auto kern = grouped_gemm_bf16_kernel<MODE, EPI, BN, A_MN, B_MN, CG>;
-  const int smem = Smem<BN, CG>::kAlloc;
+  const int smem = Smem<BN, CG, EPI != EPI_STORE>::kAlloc;
+  const CUtensorMap& mc = tc ? *tc : tb;  // the plain epilogue uses neither
+  const CUtensorMap& md = td ? *td : tb;
   static bool attr_set = false;
   static int max_units = 0;  // co-resident CTAs (CG = 1) or CTA pairs (CG = 2)
   if (!attr_set) {
@@ -619,7 +790,7 @@ static int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
   long long units = tiles_bound < max_units ? tiles_bound : max_units;
   if (units < 1) units = 1;
   if (CG == 1) {
-    kern<<<(unsigned)units, kThreads, smem, st>>>(ta, tb, p);
+    kern<<<(unsigned)units, kThreads, smem, st>>>(ta, tb, mc, md, p);
     return launch_status();
   }
   cudaLaunchConfig_t cfg = {};
@@ -634,7 +805,7 @@ static int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, p) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, mc, md, p) != cudaSuccess) return MOE_ERR_CUDA;
   return launch_status();
 }
 
@@ -723,14 +894,19 @@ extern "C" int moe_fc1_swiglu_bf16(const void* xp, const void* w1, const int32_t
   p.p_rows = p_rows;
   p.GU = static_cast<__nv_bfloat16*>(gu);
   p.Hout = static_cast<__nv_bfloat16*>(h);
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc, td;
   if (!make_tmap(&ta, xp, kBF16, 2, rows, H, H, BM, BK, kKSwz)) return MOE_ERR_CUDA;
   if (!make_tmap(&tb, w1, kBF16, 2, (long long)E * H, 2 * F, 2 * F, BK, 64)) return MOE_ERR_CUDA;
+  // [g | u] and H stored in 32 x 32 boxes
+  if (!make_tmap(&tc, gu, kBF16, 2, rows, 2LL * F, 2LL * F, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_tmap(&td, h, kBF16, 2, rows, F, F, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return MOE_ERR_CUDA;
   long long bound_base = rows / BM + E;
   cudaStream_t st = (cudaStream_t)stream;
   if (F % 128 == 0)
-    return launch<FPROP, EPI_SWIGLU_FWD, 256, 0, 1, 2>(ta, tb, p, bound_base * (F / 128), st);
-  return launch<FPROP, EPI_SWIGLU_FWD, 128, 0, 1>(ta, tb, p, bound_base * (F / 64), st);
+    return launch<FPROP, EPI_SWIGLU_FWD, 256, 0, 1, 2>(ta, tb, p, bound_base * (F / 128), st,
+                                                        &tc, &td);
+  return launch<FPROP, EPI_SWIGLU_FWD, 128, 0, 1>(ta, tb, p, bound_base * (F / 64), st, &tc, &td);
 }
 
 extern "C" int moe_swiglu_bwd_parts(int F) {
@@ -759,13 +935,17 @@ extern "C" int moe_fc2_dgrad_swiglu_bwd_bf16(const void* dy2, const void* w2,
   p.dp_part = dp_part;
   p.n_part = moe_swiglu_bwd_parts(F);
   const bool bn256 = (F % 256) == 0;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc, td;
   if (!make_tmap(&ta, dy2, kBF16, 2, rows, H, H, BM, BK, kKSwz)) return MOE_ERR_CUDA;
   // dH = dY2 * W2_e^T: B_e = W2_e stored [F, H] = [N, K], K-major.
   if (!make_tmap(&tb, w2, kBF16, 2, (long long)E * F, H, H, bn256 ? 128 : 64, BK, kKSwz))
     return MOE_ERR_CUDA;
+  // saved [g | u] read, dY1 stored, in 32 x 32 boxes
+  if (!make_tmap(&tc, gu, kBF16, 2, rows, 2LL * F, 2LL * F, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_tmap(&td, dy1, kBF16, 2, rows, 2LL * F, 2LL * F, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return MOE_ERR_CUDA;
   long long bound = (rows / BM + E) * (long long)(F / 128);
   cudaStream_t st = (cudaStream_t)stream;
-  return bn256 ? launch<FPROP, EPI_SWIGLU_BWD, 256, 0, 0, 2>(ta, tb, p, bound, st)
-               : launch<FPROP, EPI_SWIGLU_BWD, 128, 0, 0>(ta, tb, p, bound, st);
+  return bn256 ? launch<FPROP, EPI_SWIGLU_BWD, 256, 0, 0, 2>(ta, tb, p, bound, st, &tc, &td)
+               : launch<FPROP, EPI_SWIGLU_BWD, 128, 0, 0>(ta, tb, p, bound, st, &tc, &td);
 }
