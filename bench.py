@@ -136,7 +136,7 @@ class Step:
     moe_layer_backward make, over the same workspace, with optional CUDA events
     between calls for the per-kernel breakdown."""
 
-    def __init__(self, wl, dev, router=False):
+    def __init__(self, wl, dev, router=False, gather=False):
         from mixture_experts_expert_sort_b300 import binding as B
         from mixture_experts_expert_sort_b300.layer import MoELayer
         self.B = B
@@ -144,6 +144,9 @@ class Step:
         self.router = router
         self.mx = wl.precision in ("mxfp8", "mxfp8_act4")
         self.act4 = wl.precision == "mxfp8_act4"
+        # BF16 only: read x and dOut through row gathers instead of the
+        # permuted copies the layer makes (a comparison, not the layer's sequence)
+        self.gather = gather and not self.mx
         self.layer = MoELayer(wl.T, wl.H, wl.F, wl.E, wl.k, precision=wl.precision,
                               align=wl.align, device=dev)
         L = self.layer
@@ -186,16 +189,45 @@ class Step:
                 p(P["idx"]), T, E, k, wl.align, p(P["counts"]), p(P["offsets"]), p(P["dest"]),
                 p(P["src"]), R, p(self.plan_ws), self.plan_ws.numel(), s)),
         ]
-        if not self.mx:
+        if self.gather:
+            import ctypes
+            g = ctypes.byref(B.RowGather(p(P["src"]), k, T))
+            ops += [
+                ("p_rows", lambda: L.moe_permute(
+                    p(x), p(P["dest"]), p(P["offsets"]), p(P["counts"]), p(P["w"]), T, H, E, k,
+                    None, p(P["p_rows"]), s)),
+                ("fc1_swiglu", lambda: L.moe_fc1_swiglu_bf16(
+                    p(x), p(w1), p(P["offsets"]), p(P["p_rows"]), E, R, H, F, p(P["gu"]),
+                    p(P["h"]), g, s)),
+                ("fc2", lambda: L.moe_grouped_gemm_bf16(
+                    0, p(P["h"]), p(w2), 0, p(P["offsets"]), E, R, 0, H, F, p(P["y2"]), None,
+                    None, s)),
+                ("unpermute", lambda: L.moe_unpermute(p(P["y2"]), p(P["dest"]), None, T, H, k,
+                                                      p(out), s)),
+                ("fc2_dgrad_swiglu_bwd", lambda: L.moe_fc2_dgrad_swiglu_bwd_bf16(
+                    p(dout), p(w2), p(P["offsets"]), p(P["p_rows"]), p(P["gu"]), E, R, H, F,
+                    p(P["dy1"]), p(P["dp"]), g, s)),
+                ("fc2_wgrad", lambda: L.moe_grouped_gemm_bf16(
+                    1, p(P["h"]), p(dout), 0, p(P["offsets"]), E, R, F, H, 0, p(dw2), None, g,
+                    s)),
+                ("fc1_dgrad", lambda: L.moe_grouped_gemm_bf16(
+                    0, p(P["dy1"]), p(w1), 1, p(P["offsets"]), E, R, 0, H, 2 * F, p(P["dxp"]),
+                    None, None, s)),
+                ("fc1_wgrad", lambda: L.moe_grouped_gemm_bf16(
+                    1, p(x), p(P["dy1"]), 0, p(P["offsets"]), E, R, H, 2 * F, 0, p(dw1), g, None,
+                    s)),
+            ]
+        elif not self.mx:
             ops += [
                 ("permute_x", lambda: L.moe_permute(
                     p(x), p(P["dest"]), p(P["offsets"]), p(P["counts"]), p(P["w"]), T, H, E, k,
                     p(P["xp"]), p(P["p_rows"]), s)),
                 ("fc1_swiglu", lambda: L.moe_fc1_swiglu_bf16(
                     p(P["xp"]), p(w1), p(P["offsets"]), p(P["p_rows"]), E, R, H, F, p(P["gu"]),
-                    p(P["h"]), s)),
+                    p(P["h"]), None, s)),
                 ("fc2", lambda: L.moe_grouped_gemm_bf16(
-                    0, p(P["h"]), p(w2), 0, p(P["offsets"]), E, R, 0, H, F, p(P["y2"]), s)),
+                    0, p(P["h"]), p(w2), 0, p(P["offsets"]), E, R, 0, H, F, p(P["y2"]), None,
+                    None, s)),
                 ("unpermute", lambda: L.moe_unpermute(p(P["y2"]), p(P["dest"]), None, T, H, k,
                                                       p(out), s)),
                 ("permute_dout", lambda: L.moe_permute(
@@ -203,15 +235,16 @@ class Step:
                     p(P["dy2"]), None, s)),
                 ("fc2_dgrad_swiglu_bwd", lambda: L.moe_fc2_dgrad_swiglu_bwd_bf16(
                     p(P["dy2"]), p(w2), p(P["offsets"]), p(P["p_rows"]), p(P["gu"]), E, R, H, F,
-                    p(P["dy1"]), p(P["dp"]), s)),
+                    p(P["dy1"]), p(P["dp"]), None, s)),
                 ("fc2_wgrad", lambda: L.moe_grouped_gemm_bf16(
-                    1, p(P["h"]), p(P["dy2"]), 0, p(P["offsets"]), E, R, F, H, 0, p(dw2), s)),
+                    1, p(P["h"]), p(P["dy2"]), 0, p(P["offsets"]), E, R, F, H, 0, p(dw2), None,
+                    None, s)),
                 ("fc1_dgrad", lambda: L.moe_grouped_gemm_bf16(
                     0, p(P["dy1"]), p(w1), 1, p(P["offsets"]), E, R, 0, H, 2 * F, p(P["dxp"]),
-                    s)),
+                    None, None, s)),
                 ("fc1_wgrad", lambda: L.moe_grouped_gemm_bf16(
                     1, p(P["xp"]), p(P["dy1"]), 0, p(P["offsets"]), E, R, H, 2 * F, 0, p(dw1),
-                    s)),
+                    None, None, s)),
             ]
         else:
             def q(name):
@@ -534,7 +567,7 @@ def timed_steps(args, wl, world, local, dev):
          "dw1": torch.empty((E, H, 2 * F), dtype=bf, device=dev),
          "dw2": torch.empty((E, F, H), dtype=bf, device=dev),
          "dlogits": torch.empty((T, E), dtype=torch.float32, device=dev)}
-    step = Step(wl, dev, router=args.router)
+    step = Step(wl, dev, router=args.router, gather=args.gather_operands)
     step.bind(t["logits"], t["x"], t["w1"], t["w2"], t["dout"], t["out"], t["dx"], t["dw1"],
               t["dw2"], t["dlogits"])
     for _ in range(args.warmup):
@@ -724,7 +757,10 @@ def run_ours(args, wl, world, rank, local):
         "dtype": dtype_of(wl), "data": "synthetic (seeded, generated on the device)",
         "config": dict(config_of(wl), router=("router projection x W_r, top-k, aux "
                                               "load-balancing loss and their backward included"
-                                              if args.router else "logits given (no router)")),
+                                              if args.router else "logits given (no router)"),
+                       **({"operands": "x and dOut read through row gathers (tile::gather4), "
+                                       "no permuted copies; e2e still uses the layer's copies"}
+                          if args.gather_operands and not is_mx(wl) else {})),
         "gemm_tflops": head["gemm_tflops"],
         "gemm_frac_of_peak": head["gemm_frac_of_peak"],
         "gemm_frac_of_spec": head["gemm_frac_of_spec"],
@@ -834,6 +870,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling cases)")
     ap.add_argument("--experts", type=int, default=0, help="override E (profiling cases)")
+    ap.add_argument("--gather-operands", action="store_true",
+                    help="BF16: time the step with x and dOut read through row gathers "
+                         "instead of the layer's permuted copies")
     ap.add_argument("--router", action="store_true",
                     help="compute the logits with the router projection (x W_r) and add the "
                          "aux load-balancing loss and the router backward to the step")

@@ -54,7 +54,7 @@ enum moe_status {
 };
 
 /* Device error word flags (moe_device_error). */
-#define MOE_DEVERR_BAD_INDEX 0x1u   /* an expert index outside [0, E) */
+#define MOE_DEVERR_BAD_INDEX 0x1u   /* an expert index outside [0, E), or a gathered row past its source */
 #define MOE_DEVERR_TIMEOUT 0x2u     /* a bounded wait in a pipelined kernel gave up */
 #define MOE_DEVERR_CAPACITY 0x4u    /* more padded rows than the buffer holds */
 #define MOE_DEVERR_LAYOUT 0x8u      /* group offsets not aligned as the call requires */
@@ -339,12 +339,33 @@ MOE_API int mxfp8_colwise_from_mxfp4_rowwise(const uint8_t* q4, const uint8_t* s
  *   Experts with no rows get C_e = 0. Requires M % 128 == 0, N % 128 == 0,
  *   and every group size a multiple of 64 (else MOE_DEVERR_LAYOUT).
  * All of A, B, C 16-byte aligned; 1 <= E <= 256; rows < 2^31.
+ *
+ * Row gather (the permute-free operands of "Efficient MoE Training ...",
+ * §Challenge 3: the fused path "avoids materializing some intermediate
+ * results"): an operand whose rows are the permuted rows can instead be
+ * read straight from its un-permuted source. With a moe_row_gather g, row r
+ * of the operand is row g.src[r] / g.src_div of the source tensor (which has
+ * g.src_rows rows and the operand's columns), and a zero row where
+ * g.src[r] < 0 (padding). g.src is moe_permute_plan's src map (src_div = k),
+ * at least `rows` entries. The source pointer is passed in place of the
+ * operand, 16-byte aligned. Requires src_rows < 2^31, src_div >= 1. A source
+ * row >= src_rows is read as a zero row and sets MOE_DEVERR_BAD_INDEX.
+ * The gathered rows are copied into the GEMM's shared-memory stages by
+ * 16-byte asynchronous copies, the other operand by TMA.
  */
 #define MOE_GEMM_FPROP 0
 #define MOE_GEMM_WGRAD 1
+typedef struct moe_row_gather {
+  const int32_t* src;  /* device, [rows]: flat routed index of each permuted row, -1 padding */
+  int src_div;         /* source row = src[r] / src_div */
+  long long src_rows;  /* rows of the source tensor */
+} moe_row_gather;
+/* ga, gb: optional gathers of A and B (NULL: the operand is stored permuted).
+ * FPROP gathers only A (gb must be NULL); WGRAD may gather either operand. */
 MOE_API int moe_grouped_gemm_bf16(int mode, const void* A, const void* B, int b_layout,
                                   const int32_t* offsets, int E, long long rows, int M, int N,
-                                  int K, void* C, moe_stream_t stream);
+                                  int K, void* C, const moe_row_gather* ga,
+                                  const moe_row_gather* gb, moe_stream_t stream);
 
 /* moe_fc1_swiglu_bf16: the fused gate_up GroupedLinear + ScaledSwiGLU of
  * "Efficient MoE Training ...", §Challenge 3. For every row r of group e:
@@ -353,10 +374,11 @@ MOE_API int moe_grouped_gemm_bf16(int mode, const void* A, const void* B, int b_
  *   h[r, f] = silu(g_f) * u_f * p_rows[r]  (bf16), silu(z) = z / (1 + e^-z).
  *   xp [rows, H], w1 [E, H, 2F], gu [rows, 2F], h [rows, F] bf16;
  *   p_rows [rows] fp32 (moe_permute's per-row routing weight).
+ *   gx: optional row gather of xp (xp is then the tokens x [src_rows, H]).
  * Requires H % 64 == 0, F % 64 == 0. */
 MOE_API int moe_fc1_swiglu_bf16(const void* xp, const void* w1, const int32_t* offsets,
                                 const float* p_rows, int E, long long rows, int H, int F,
-                                void* gu, void* h, moe_stream_t stream);
+                                void* gu, void* h, const moe_row_gather* gx, moe_stream_t stream);
 
 /* moe_swiglu_bwd_parts: number of partial sums per row that
  * moe_fc2_dgrad_swiglu_bwd_bf16 writes to dp_part (0 if F is unsupported). */
@@ -369,11 +391,14 @@ MOE_API int moe_swiglu_bwd_parts(int F);
  *   dp_part[r, c] = sum over the c-th block of F columns of dH*a (fp32),
  *   c < moe_swiglu_bwd_parts(F); sum them with moe_route_backward.
  * silu'(z) = s(z)*(1 + z*(1 - s(z))), s the logistic function.
+ * gdy: optional row gather of dy2 (dy2 is then the upstream gradient
+ * [src_rows, H] in token order).
  * Requires H % 64 == 0, F % 128 == 0. */
 MOE_API int moe_fc2_dgrad_swiglu_bwd_bf16(const void* dy2, const void* w2,
                                           const int32_t* offsets, const float* p_rows,
                                           const void* gu, int E, long long rows, int H, int F,
-                                          void* dy1, float* dp_part, moe_stream_t stream);
+                                          void* dy1, float* dp_part, const moe_row_gather* gdy,
+                                          moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * MXFP8 grouped GEMMs on the block-scaled tcgen05 MMA ("Efficient MoE
@@ -454,7 +479,10 @@ MOE_API int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t* s
  *   Must follow moe_layer_forward with the same cfg, weights and workspace.
  * Precision:
  *   MOE_PRECISION_BF16: bf16 operands, fp32 accumulation; [g|u], H and the
- *     permuted activations are kept in bf16.
+ *     permuted activations are kept in bf16. The permuted copies of x and
+ *     dOut are made by moe_permute rather than read through row gathers
+ *     (moe_row_gather): a gathered GEMM operand costs one TMA request per
+ *     four 128-byte rows, far more time than the copy.
  *   MOE_PRECISION_MXFP8 (§Challenge 2 and 3): x, W1, W2 and dOut are
  *     quantised to MXFP8 (the permutes of x and dOut are fused into their
  *     quantisation; both weights are quantised once per forward, row- and

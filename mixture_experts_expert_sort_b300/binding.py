@@ -27,6 +27,15 @@ GEMM_FPROP, GEMM_WGRAD = 0, 1
 
 _p, _i, _ll, _sz, _u = C.c_void_p, C.c_int, C.c_longlong, C.c_size_t, C.c_uint
 
+
+class RowGather(C.Structure):
+    """moe_row_gather: permuted row r reads source row src[r] // src_div
+    (src[r] < 0: a zero row); src_rows is the source tensor's row count."""
+    _fields_ = [("src", _p), ("src_div", _i), ("src_rows", _ll)]
+
+
+_g = C.POINTER(RowGather)
+
 # name -> (restype, argtypes); mirrors include/moe.h
 SIGNATURES = {
     "moe_status_string": (C.c_char_p, [_i]),
@@ -46,10 +55,11 @@ SIGNATURES = {
     "mxfp8_from_mxfp4": (_i, [_p, _p, _ll, _i, _p, _p, _p]),
     "mxfp4_rowwise_to_colwise": (_i, [_p, _p, _ll, _i, _p, _p, _p]),
     "mxfp8_colwise_from_mxfp4_rowwise": (_i, [_p, _p, _ll, _i, _p, _p, _p]),
-    "moe_grouped_gemm_bf16": (_i, [_i, _p, _p, _i, _p, _i, _ll, _i, _i, _i, _p, _p]),
-    "moe_fc1_swiglu_bf16": (_i, [_p, _p, _p, _p, _i, _ll, _i, _i, _p, _p, _p]),
+    "moe_grouped_gemm_bf16": (_i, [_i, _p, _p, _i, _p, _i, _ll, _i, _i, _i, _p, _g, _g, _p]),
+    "moe_fc1_swiglu_bf16": (_i, [_p, _p, _p, _p, _i, _ll, _i, _i, _p, _p, _g, _p]),
     "moe_swiglu_bwd_parts": (_i, [_i]),
-    "moe_fc2_dgrad_swiglu_bwd_bf16": (_i, [_p, _p, _p, _p, _p, _i, _ll, _i, _i, _p, _p, _p]),
+    "moe_fc2_dgrad_swiglu_bwd_bf16": (_i, [_p, _p, _p, _p, _p, _i, _ll, _i, _i, _p, _p, _g,
+                                           _p]),
     "moe_grouped_gemm_mxfp8": (_i, [_i, _p, _p, _ll, _ll, _p, _p, _ll, _ll, _ll, _ll, _p, _i,
                                     _i, _i, _i, _p, _p]),
     "moe_fc1_swiglu_mxfp8": (_i, [_p, _p, _ll, _i, _p, _p, _p, _p, _i, _i, _p, _p, _p, _p, _p,
@@ -393,11 +403,26 @@ def mxfp8_colwise_from_mxfp4_rowwise(q4, s4, stream=None, out=None):
 
 # ----------------------------------------------------------- grouped GEMM
 
-def moe_grouped_gemm_bf16(mode, A, B, offsets, b_layout=0, M=0, N=0, K=0, C=None, stream=None):
+def _row_gather(gather, source):
+    """(src, src_div) -> (RowGather over `source`'s rows, or None; the number
+    of permuted rows, src.numel(), or None)."""
+    if gather is None:
+        return None, None
+    src, src_div = gather
+    g = RowGather(ptr(src, I32), int(src_div), int(source.shape[0]))
+    return C.byref(g), src.numel()
+
+
+def moe_grouped_gemm_bf16(mode, A, B, offsets, b_layout=0, M=0, N=0, K=0, C=None, stream=None,
+                          gather_a=None, gather_b=None):
     """FPROP: C[rows, N] = A[rows] @ B_e per group (B [E,K,N] or [E,N,K]).
-    WGRAD: C[E, M, N] = A_e^T @ B_e over each group's rows (A [rows, M], B [rows, N])."""
+    WGRAD: C[E, M, N] = A_e^T @ B_e over each group's rows (A [rows, M], B [rows, N]).
+    gather_a / gather_b = (src, src_div): that operand is its un-permuted source
+    and permuted row r is its row src[r] // src_div (rows = src.numel())."""
     E = offsets.numel() - 1
-    rows = A.shape[0]
+    ga, ra = _row_gather(gather_a, A)
+    gb, rb = _row_gather(gather_b, B)
+    rows = ra if ra is not None else rb if rb is not None else A.shape[0]
     if mode == GEMM_FPROP:
         K = A.shape[1]
         N = B.shape[2] if b_layout == 0 else B.shape[1]
@@ -406,20 +431,24 @@ def moe_grouped_gemm_bf16(mode, A, B, offsets, b_layout=0, M=0, N=0, K=0, C=None
         M, N = A.shape[1], B.shape[1]
         C = C if C is not None else torch.empty((E, M, N), dtype=torch.bfloat16, device=A.device)
     _check(lib().moe_grouped_gemm_bf16(mode, ptr(A, BF16), ptr(B, BF16), b_layout,
-                                       ptr(offsets, I32), E, rows, M, N, K, ptr(C, BF16),
+                                       ptr(offsets, I32), E, rows, M, N, K, ptr(C, BF16), ga, gb,
                                        stream_handle(stream)), "moe_grouped_gemm_bf16")
     return C
 
 
-def moe_fc1_swiglu_bf16(xp, w1, offsets, p_rows, gu=None, h=None, stream=None):
-    rows, H = xp.shape
+def moe_fc1_swiglu_bf16(xp, w1, offsets, p_rows, gu=None, h=None, stream=None, gather_x=None):
+    """gather_x = (src, src_div): xp is the un-permuted x and permuted row r is
+    its row src[r] // src_div (rows = src.numel())."""
+    gx, rows = _row_gather(gather_x, xp)
+    H = xp.shape[1]
+    rows = rows if rows is not None else xp.shape[0]
     E, _, F2 = w1.shape
     F = F2 // 2
     gu = gu if gu is not None else torch.empty((rows, F2), dtype=torch.bfloat16, device=xp.device)
     h = h if h is not None else torch.empty((rows, F), dtype=torch.bfloat16, device=xp.device)
     _check(lib().moe_fc1_swiglu_bf16(ptr(xp, BF16), ptr(w1, BF16), ptr(offsets, I32),
                                      ptr(p_rows, F32), E, rows, H, F, ptr(gu, BF16), ptr(h, BF16),
-                                     stream_handle(stream)), "moe_fc1_swiglu_bf16")
+                                     gx, stream_handle(stream)), "moe_fc1_swiglu_bf16")
     return gu, h
 
 
@@ -428,8 +457,12 @@ def moe_swiglu_bwd_parts(F):
 
 
 def moe_fc2_dgrad_swiglu_bwd_bf16(dy2, w2, offsets, p_rows, gu, dy1=None, dp_part=None,
-                                  stream=None):
-    rows, H = dy2.shape
+                                  stream=None, gather_dy=None):
+    """gather_dy = (src, src_div): dy2 is the un-permuted dOut and permuted row
+    r is its row src[r] // src_div (rows = src.numel())."""
+    gdy, rows = _row_gather(gather_dy, dy2)
+    H = dy2.shape[1]
+    rows = rows if rows is not None else dy2.shape[0]
     E, F, _ = w2.shape
     dev = dy2.device
     dy1 = dy1 if dy1 is not None else torch.empty((rows, 2 * F), dtype=torch.bfloat16, device=dev)
@@ -437,7 +470,7 @@ def moe_fc2_dgrad_swiglu_bwd_bf16(dy2, w2, offsets, p_rows, gu, dy1=None, dp_par
         dp_part = torch.empty((rows, moe_swiglu_bwd_parts(F)), dtype=torch.float32, device=dev)
     _check(lib().moe_fc2_dgrad_swiglu_bwd_bf16(ptr(dy2, BF16), ptr(w2, BF16), ptr(offsets, I32),
                                                ptr(p_rows, F32), ptr(gu, BF16), E, rows, H, F,
-                                               ptr(dy1, BF16), ptr(dp_part, F32),
+                                               ptr(dy1, BF16), ptr(dp_part, F32), gdy,
                                                stream_handle(stream)),
            "moe_fc2_dgrad_swiglu_bwd_bf16")
     return dy1, dp_part

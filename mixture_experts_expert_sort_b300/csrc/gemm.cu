@@ -65,6 +65,14 @@ struct Params {
   __nv_bfloat16* Hout;       // FWD: out [rows, F]
   float* dp_part;            // BWD: [rows, n_part] partial dL/dp per n-tile
   int n_part;
+  // Row gather of one operand (template parameter G): permuted row r is row
+  // g_src[r] / g_div of the source (g_rows rows, read through a tensor map
+  // with one-row boxes), or zeros where g_src[r] < 0 or r >= g_n. A source
+  // row past g_rows is read as zeros and reported as MOE_DEVERR_BAD_INDEX.
+  long long g_rows;
+  const int32_t* g_src;
+  int g_div;
+  long long g_n;
 };
 
 // CG = 2: a CTA pair shares each tile (M = 256), each CTA staging its own 128
@@ -74,14 +82,17 @@ struct Params {
 // receives gate and up and stages dg and du).
 constexpr int kEpiBufBytes = 8192;
 
-template <int BN, int CG = 1, bool FUSED = false>
+// GATHER: the producer keeps the source row of each gathered operand row of
+// a tile (FPROP, 128) or stage (WGRAD, 64) in shared memory.
+template <int BN, int CG = 1, bool FUSED = false, bool GATHER = false>
 struct Smem {
   static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = (BN / CG) * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (CG == 2 || BN != 256) ? 6 : 4;
   static constexpr int kEpiOffset = kStages * kStageBytes;  // 1024-byte aligned
-  static constexpr int kBarOffset = kEpiOffset + (FUSED ? 4 * kEpiBufBytes : 0);
+  static constexpr int kGatherOffset = kEpiOffset + (FUSED ? 4 * kEpiBufBytes : 0);
+  static constexpr int kBarOffset = kGatherOffset + (GATHER ? BM * 4 : 0);
   // full[S], empty[S], tfull[2], tempty[2], drain, gate/up loads[4]
   static constexpr int kNumBars = 2 * kStages + 5 + (FUSED ? 4 : 0);
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
@@ -239,14 +250,16 @@ __device__ __forceinline__ void load_gate_up(const CUtensorMap* tm, uint32_t dst
 // boxes by TMA: FC1 + SwiGLU stores [g | u] (tmC) and H (tmD); FC2 dgrad +
 // SwiGLU backward reads the saved [g | u] (tmC) and stores dY1 (tmD). A warp
 // whose 32 rows straddle the end of a group uses per-lane loads and stores.
-template <int MODE, int EPI, int BN, int A_MN, int B_MN, int CG>
+// G: which operand is read through a row gather (tmA or tmB is then a map of
+// the un-permuted source with one-row boxes): 0 none, 1 A, 2 B (WGRAD only).
+template <int MODE, int EPI, int BN, int A_MN, int B_MN, int CG, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmC,
                              const __grid_constant__ CUtensorMap tmD, const Params p) {
   constexpr bool kFused = EPI != EPI_STORE;
-  using L = Smem<BN, CG, kFused>;
+  using L = Smem<BN, CG, kFused, G != 0>;
   constexpr bool kPair = CG == 2;
   // Rows of A (and columns of B) this CTA stages per stage, and the tile's M.
   constexpr int kTileM = BM * CG;
@@ -335,7 +348,138 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *s_tmem;
   const int total_tiles = s_prefix[p.E];
 
-  if (warp == 0) {
+  if (warp == 0 && G != 0) {
+    // ------------------------------------------------- producer, row gather
+    // The whole warp looks up the source row of every gathered operand row
+    // (the tile's 128 A rows once per tile in FPROP, the stage's 64 reduction
+    // rows in WGRAD, prefetched a stage ahead) into shared memory; lane 0
+    // arms the stage and issues the other operand's box loads, and each lane
+    // issues a tile::gather4 of four 128-byte rows. Every such TMA request
+    // moves 512 bytes, so the gathered stream runs at the TMA unit's request
+    // rate rather than at the bandwidth a 16 KB box load reaches.
+    int* s_grow = reinterpret_cast<int*>(smem + L::kGatherOffset);
+    // source row of a src entry; rows past the source (g_rows) are the
+    // tensor map's zero fill, and a src entry past it is also reported
+    auto src_row = [&](int sv) -> int {
+      if (sv < 0) return (int)p.g_rows;
+      const int r = sv / p.g_div;
+      if (r >= p.g_rows) {
+        raise_device_error(MOE_DEVERR_BAD_INDEX);
+        return (int)p.g_rows;
+      }
+      return r;
+    };
+    auto raw_src = [&](long long r) -> int { return r < p.g_n ? p.g_src[r] : -1; };
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed_phase[L::kStages];
+    bool armed[L::kStages];
+    for (int s = 0; s < L::kStages; ++s) armed[s] = false;
+    int e_hint = 0;
+    bool ok = true;
+    for (int t = unit; t < total_tiles && ok; t += n_units) {
+      TileInfo ti;
+      decode_tile<MODE, BN, CG>(p, s_prefix, t, e_hint, ti);
+      int nx0 = 0, nx1 = 0;  // WGRAD: src entries of the next stage's rows
+      if (MODE == FPROP) {
+        const long long r0 = ti.row0 + (long long)ti.mt * kTileM + (long long)rank * BM;
+        __syncwarp();  // the previous tile's copies are issued
+        for (int i = lane; i < BM; i += 32) s_grow[i] = src_row(raw_src(r0 + i));
+        __syncwarp();
+      } else {
+        nx0 = raw_src(ti.row0 + lane);
+        nx1 = raw_src(ti.row0 + 32 + lane);
+      }
+      for (int kb = 0; kb < ti.k_iters; ++kb) {
+        if (lane == 0) ok = wait_bar(empty_bar(stage), phase ^ 1u, s_abort);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const int k0 = kb * BK;
+        if (MODE == WGRAD) {
+          __syncwarp();  // the previous stage's copies are issued
+          s_grow[lane] = src_row(nx0);
+          s_grow[lane + 32] = src_row(nx1);
+          if (kb + 1 < ti.k_iters) {  // prefetch the next stage's entries
+            nx0 = raw_src(ti.row0 + k0 + BK + lane);
+            nx1 = raw_src(ti.row0 + k0 + BK + 32 + lane);
+          }
+        }
+        const uint32_t a_dst = sbase + stage * L::kStageBytes;
+        const uint32_t b_dst = a_dst + L::kABytes;
+        const uint32_t fb = kPair ? ptx::mapa_shared(full_bar(stage), 0) : full_bar(stage);
+        if (lane == 0 && rank == 0) {
+          ptx::mbar_arrive_expect_tx(full_bar(stage), CG * L::kStageBytes);
+          armed[stage] = true;
+          armed_phase[stage] = phase;
+        }
+        __syncwarp();  // the stage is armed (and s_grow written) before any copy
+        auto load = [&](uint32_t dst, const CUtensorMap* tm, int c0, int c1) {
+          if (kPair)
+            ptx::tma_load_2d_cg2(dst, tm, c0, c1, fb);
+          else
+            ptx::tma_load_2d(dst, tm, c0, c1, fb);
+        };
+        // n_rows gathered rows (s_grow[0 .. n_rows)) of columns c0 .. c0+63
+        // to dst, one tile::gather4 of four rows per lane
+        auto gather = [&](uint32_t dst, const CUtensorMap* tm, int c0, int n_rows) {
+          for (int i = lane; i < n_rows / 4; i += 32) {
+            const int* rr = s_grow + 4 * i;
+            if (kPair)
+              ptx::tma_gather4_cg2(dst + i * 512, tm, c0, rr[0], rr[1], rr[2], rr[3], fb);
+            else
+              ptx::tma_gather4(dst + i * 512, tm, c0, rr[0], rr[1], rr[2], rr[3], fb);
+          }
+        };
+        if (MODE == FPROP) {
+          gather(a_dst, &tmA, k0, BM);  // A: this CTA's 128 rows, K-major
+          if (lane == 0) {
+            if (B_MN) {
+#pragma unroll
+              for (int c = 0; c < kBCols / 64; ++c) {
+                const int cc = (int)rank * (kBCols / 64) + c;
+                const int h = cc / (BN / 128), off = (cc % (BN / 128)) * 64;
+                const int n = b_half_col<EPI, BN>(p, ti.nt, h) + off;
+                load(b_dst + c * (BK * 128), &tmB, n, ti.e * p.K + k0);
+              }
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2 / CG; ++h) {
+                const int n = b_half_col<EPI, BN>(p, ti.nt, kPair ? (int)rank : h);
+                load(b_dst + h * (BN / 2) * kKRowBytes, &tmB, k0, ti.e * p.N + n);
+              }
+            }
+          }
+        } else {
+          // WGRAD: the gathered operand's 64 reduction rows are s_grow[0 .. 64)
+          const int r = (int)(ti.row0 + k0);
+#pragma unroll
+          for (int c = 0; c < BM / 64; ++c) {
+            const int m = ti.mt * kTileM + (int)rank * BM + c * 64;
+            if (G == 1)
+              gather(a_dst + c * (BK * 128), &tmA, m, BK);
+            else if (lane == 0)
+              load(a_dst + c * (BK * 128), &tmA, m, r);
+          }
+#pragma unroll
+          for (int c = 0; c < kBCols / 64; ++c) {
+            const int n = ti.nt * BN + (int)rank * kBCols + c * 64;
+            if (G == 2)
+              gather(b_dst + c * (BK * 128), &tmB, n, BK);
+            else if (lane == 0)
+              load(b_dst + c * (BK * 128), &tmB, n, r);
+          }
+        }
+        if (++stage == L::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // Let every armed copy land before the CTA can exit (bounded).
+    if (lane == 0)
+      for (int s = 0; s < L::kStages; ++s)
+        if (armed[s]) drain_wait(full_bar(s), armed_phase[s]);
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (ptx::elect_one()) {
       int stage = 0;
@@ -754,12 +898,12 @@ static int num_sms() {
 
 // tiles_bound: an upper bound on the tiles of the launch (for CG = 2, on the
 // 256-row tiles that CTA pairs take).
-template <int MODE, int EPI, int BN, int A_MN, int B_MN, int CG = 1>
+template <int MODE, int EPI, int BN, int A_MN, int B_MN, int CG = 1, int G = 0>
 static int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
                   long long tiles_bound, cudaStream_t st, const CUtensorMap* tc = nullptr,
                   const CUtensorMap* td = nullptr) {
-  auto kern = grouped_gemm_bf16_kernel<MODE, EPI, BN, A_MN, B_MN, CG>;
-  const int smem = Smem<BN, CG, EPI != EPI_STORE>::kAlloc;
+  auto kern = grouped_gemm_bf16_kernel<MODE, EPI, BN, A_MN, B_MN, CG, G>;
+  const int smem = Smem<BN, CG, EPI != EPI_STORE, G != 0>::kAlloc;
   const CUtensorMap& mc = tc ? *tc : tb;  // the plain epilogue uses neither
   const CUtensorMap& md = td ? *td : tb;
   static bool attr_set = false;
@@ -822,12 +966,33 @@ bool gemm_common_ok(const void* A, const void* B, const void* C, const int32_t* 
   return A && B && C && offsets && E >= 1 && E <= kMaxGroups && aligned16(A) && aligned16(B) &&
          aligned16(C);
 }
+
+// A row gather, when given, must name its map and a source of 1 .. 2^31-1 rows.
+bool gather_ok(const moe_row_gather* g) {
+  return !g || (g->src && g->src_div >= 1 && g->src_rows >= 1 && g->src_rows < (1LL << 31));
+}
+
+// The gathered operand [src_rows, cols] at base: permuted row r < rows is its
+// row src[r] / src_div (zeros where src[r] < 0), read through a map of
+// one-row boxes of 64 columns (128 bytes, 128-byte swizzle), four rows per
+// tile::gather4.
+bool set_gather(Params& p, CUtensorMap* m, const void* base, long long cols,
+                const moe_row_gather* g, long long rows) {
+  p.g_rows = g->src_rows;
+  p.g_src = g->src;
+  p.g_div = g->src_div;
+  p.g_n = rows;
+  return make_tmap(m, base, kBF16, 2, g->src_rows, cols, cols, 1, 64, kKSwz);
+}
 }  // namespace
 
 extern "C" int moe_grouped_gemm_bf16(int mode, const void* A, const void* B, int b_layout,
                                      const int32_t* offsets, int E, long long rows, int M, int N,
-                                     int K, void* C, moe_stream_t stream) {
+                                     int K, void* C, const moe_row_gather* ga,
+                                     const moe_row_gather* gb, moe_stream_t stream) {
   if (!gemm_common_ok(A, B, C, offsets, E) || rows < 0 || rows >= (1LL << 31)) return MOE_ERR_ARG;
+  if (!gather_ok(ga) || !gather_ok(gb) || (ga && gb) || (mode == MOE_GEMM_FPROP && gb))
+    return MOE_ERR_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   Params p{};
   p.offsets = offsets;
@@ -844,14 +1009,25 @@ extern "C" int moe_grouped_gemm_bf16(int mode, const void* A, const void* B, int
     p.ldc = N;
     p.b_kmajor = b_layout;
     const bool bn256 = (N % 256) == 0;
-    if (!make_tmap(&ta, A, kBF16, 2, rows, K, K, BM, BK, kKSwz)) return MOE_ERR_CUDA;
     if (b_layout == 0) {
       if (!make_tmap(&tb, B, kBF16, 2, (long long)E * K, N, N, BK, 64)) return MOE_ERR_CUDA;
     } else {
       if (!make_tmap(&tb, B, kBF16, 2, (long long)E * N, K, K, bn256 ? 128 : 64, BK, kKSwz))
         return MOE_ERR_CUDA;
     }
+    if (ga) {
+      if (!set_gather(p, &ta, A, K, ga, rows)) return MOE_ERR_CUDA;
+    } else if (!make_tmap(&ta, A, kBF16, 2, rows, K, K, BM, BK, kKSwz)) {
+      return MOE_ERR_CUDA;
+    }
     long long bound = (rows / BM + E) * (long long)(N / 128);
+    if (ga) {
+      if (bn256)
+        return b_layout ? launch<FPROP, EPI_STORE, 256, 0, 0, 2, 1>(ta, tb, p, bound, st)
+                        : launch<FPROP, EPI_STORE, 256, 0, 1, 2, 1>(ta, tb, p, bound, st);
+      return b_layout ? launch<FPROP, EPI_STORE, 128, 0, 0, 1, 1>(ta, tb, p, bound, st)
+                      : launch<FPROP, EPI_STORE, 128, 0, 1, 1, 1>(ta, tb, p, bound, st);
+    }
     if (bn256)
       return b_layout ? launch<FPROP, EPI_STORE, 256, 0, 0, 2>(ta, tb, p, bound, st)
                       : launch<FPROP, EPI_STORE, 256, 0, 1, 2>(ta, tb, p, bound, st);
@@ -864,25 +1040,40 @@ extern "C" int moe_grouped_gemm_bf16(int mode, const void* A, const void* B, int
     p.c_group_stride = (long long)M * N;
     const bool bn256 = (N % 256) == 0;
     if (rows > 0) {
-      if (!make_tmap(&ta, A, kBF16, 2, rows, M, M, BK, 64)) return MOE_ERR_CUDA;
-      if (!make_tmap(&tb, B, kBF16, 2, rows, N, N, BK, 64)) return MOE_ERR_CUDA;
+      if (ga ? !set_gather(p, &ta, A, M, ga, rows)
+             : !make_tmap(&ta, A, kBF16, 2, rows, M, M, BK, 64))
+        return MOE_ERR_CUDA;
+      if (gb ? !set_gather(p, &tb, B, N, gb, rows)
+             : !make_tmap(&tb, B, kBF16, 2, rows, N, N, BK, 64))
+        return MOE_ERR_CUDA;
     } else {
       // No rows at all: every expert's gradient is zero; maps are never read.
       if (!make_tmap(&ta, C, kBF16, 2, M, N, N, BK, 64)) return MOE_ERR_CUDA;
       tb = ta;
     }
     long long bound = (long long)E * (M / BM) * (N / 128);
-    if (bn256 && M % 256 == 0) return launch<WGRAD, EPI_STORE, 256, 1, 1, 2>(ta, tb, p, bound, st);
-    return bn256 ? launch<WGRAD, EPI_STORE, 256, 1, 1>(ta, tb, p, bound, st)
-                 : launch<WGRAD, EPI_STORE, 128, 1, 1>(ta, tb, p, bound, st);
+    const int g = rows > 0 ? (ga ? 1 : gb ? 2 : 0) : 0;
+    if (bn256 && M % 256 == 0)
+      return g == 1   ? launch<WGRAD, EPI_STORE, 256, 1, 1, 2, 1>(ta, tb, p, bound, st)
+             : g == 2 ? launch<WGRAD, EPI_STORE, 256, 1, 1, 2, 2>(ta, tb, p, bound, st)
+                      : launch<WGRAD, EPI_STORE, 256, 1, 1, 2>(ta, tb, p, bound, st);
+    if (bn256)
+      return g == 1   ? launch<WGRAD, EPI_STORE, 256, 1, 1, 1, 1>(ta, tb, p, bound, st)
+             : g == 2 ? launch<WGRAD, EPI_STORE, 256, 1, 1, 1, 2>(ta, tb, p, bound, st)
+                      : launch<WGRAD, EPI_STORE, 256, 1, 1>(ta, tb, p, bound, st);
+    return g == 1   ? launch<WGRAD, EPI_STORE, 128, 1, 1, 1, 1>(ta, tb, p, bound, st)
+           : g == 2 ? launch<WGRAD, EPI_STORE, 128, 1, 1, 1, 2>(ta, tb, p, bound, st)
+                    : launch<WGRAD, EPI_STORE, 128, 1, 1>(ta, tb, p, bound, st);
   }
   return MOE_ERR_ARG;
 }
 
 extern "C" int moe_fc1_swiglu_bf16(const void* xp, const void* w1, const int32_t* offsets,
                                    const float* p_rows, int E, long long rows, int H, int F,
-                                   void* gu, void* h, moe_stream_t stream) {
-  if (!gemm_common_ok(xp, w1, gu, offsets, E) || !h || !aligned16(h) || !p_rows) return MOE_ERR_ARG;
+                                   void* gu, void* h, const moe_row_gather* gx,
+                                   moe_stream_t stream) {
+  if (!gemm_common_ok(xp, w1, gu, offsets, E) || !h || !aligned16(h) || !p_rows || !gather_ok(gx))
+    return MOE_ERR_ARG;
   if (H < BK || H % BK || F < 64 || F % 64 || rows < 0 || rows >= (1LL << 31)) return MOE_ERR_ARG;
   if (rows == 0) return MOE_OK;
   Params p{};
@@ -895,8 +1086,12 @@ extern "C" int moe_fc1_swiglu_bf16(const void* xp, const void* w1, const int32_t
   p.GU = static_cast<__nv_bfloat16*>(gu);
   p.Hout = static_cast<__nv_bfloat16*>(h);
   CUtensorMap ta, tb, tc, td;
-  if (!make_tmap(&ta, xp, kBF16, 2, rows, H, H, BM, BK, kKSwz)) return MOE_ERR_CUDA;
   if (!make_tmap(&tb, w1, kBF16, 2, (long long)E * H, 2 * F, 2 * F, BK, 64)) return MOE_ERR_CUDA;
+  if (gx) {
+    if (!set_gather(p, &ta, xp, H, gx, rows)) return MOE_ERR_CUDA;
+  } else if (!make_tmap(&ta, xp, kBF16, 2, rows, H, H, BM, BK, kKSwz)) {
+    return MOE_ERR_CUDA;
+  }
   // [g | u] and H stored in 32 x 32 boxes
   if (!make_tmap(&tc, gu, kBF16, 2, rows, 2LL * F, 2LL * F, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_tmap(&td, h, kBF16, 2, rows, F, F, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
@@ -904,9 +1099,14 @@ extern "C" int moe_fc1_swiglu_bf16(const void* xp, const void* w1, const int32_t
   long long bound_base = rows / BM + E;
   cudaStream_t st = (cudaStream_t)stream;
   if (F % 128 == 0)
-    return launch<FPROP, EPI_SWIGLU_FWD, 256, 0, 1, 2>(ta, tb, p, bound_base * (F / 128), st,
-                                                        &tc, &td);
-  return launch<FPROP, EPI_SWIGLU_FWD, 128, 0, 1>(ta, tb, p, bound_base * (F / 64), st, &tc, &td);
+    return gx ? launch<FPROP, EPI_SWIGLU_FWD, 256, 0, 1, 2, 1>(ta, tb, p, bound_base * (F / 128),
+                                                               st, &tc, &td)
+              : launch<FPROP, EPI_SWIGLU_FWD, 256, 0, 1, 2>(ta, tb, p, bound_base * (F / 128), st,
+                                                            &tc, &td);
+  return gx ? launch<FPROP, EPI_SWIGLU_FWD, 128, 0, 1, 1, 1>(ta, tb, p, bound_base * (F / 64), st,
+                                                             &tc, &td)
+            : launch<FPROP, EPI_SWIGLU_FWD, 128, 0, 1>(ta, tb, p, bound_base * (F / 64), st, &tc,
+                                                       &td);
 }
 
 extern "C" int moe_swiglu_bwd_parts(int F) {
@@ -917,8 +1117,10 @@ extern "C" int moe_swiglu_bwd_parts(int F) {
 extern "C" int moe_fc2_dgrad_swiglu_bwd_bf16(const void* dy2, const void* w2,
                                              const int32_t* offsets, const float* p_rows,
                                              const void* gu, int E, long long rows, int H, int F,
-                                             void* dy1, float* dp_part, moe_stream_t stream) {
-  if (!gemm_common_ok(dy2, w2, dy1, offsets, E) || !gu || !aligned16(gu) || !p_rows || !dp_part)
+                                             void* dy1, float* dp_part, const moe_row_gather* gdy,
+                                             moe_stream_t stream) {
+  if (!gemm_common_ok(dy2, w2, dy1, offsets, E) || !gu || !aligned16(gu) || !p_rows || !dp_part ||
+      !gather_ok(gdy))
     return MOE_ERR_ARG;
   if (H < BK || H % BK || F < 128 || F % 128 || rows < 0 || rows >= (1LL << 31)) return MOE_ERR_ARG;
   if (rows == 0) return MOE_OK;
@@ -936,16 +1138,23 @@ extern "C" int moe_fc2_dgrad_swiglu_bwd_bf16(const void* dy2, const void* w2,
   p.n_part = moe_swiglu_bwd_parts(F);
   const bool bn256 = (F % 256) == 0;
   CUtensorMap ta, tb, tc, td;
-  if (!make_tmap(&ta, dy2, kBF16, 2, rows, H, H, BM, BK, kKSwz)) return MOE_ERR_CUDA;
   // dH = dY2 * W2_e^T: B_e = W2_e stored [F, H] = [N, K], K-major.
   if (!make_tmap(&tb, w2, kBF16, 2, (long long)E * F, H, H, bn256 ? 128 : 64, BK, kKSwz))
     return MOE_ERR_CUDA;
+  if (gdy) {
+    if (!set_gather(p, &ta, dy2, H, gdy, rows)) return MOE_ERR_CUDA;
+  } else if (!make_tmap(&ta, dy2, kBF16, 2, rows, H, H, BM, BK, kKSwz)) {
+    return MOE_ERR_CUDA;
+  }
   // saved [g | u] read, dY1 stored, in 32 x 32 boxes
   if (!make_tmap(&tc, gu, kBF16, 2, rows, 2LL * F, 2LL * F, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_tmap(&td, dy1, kBF16, 2, rows, 2LL * F, 2LL * F, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return MOE_ERR_CUDA;
   long long bound = (rows / BM + E) * (long long)(F / 128);
   cudaStream_t st = (cudaStream_t)stream;
+  if (gdy)
+    return bn256 ? launch<FPROP, EPI_SWIGLU_BWD, 256, 0, 0, 2, 1>(ta, tb, p, bound, st, &tc, &td)
+                 : launch<FPROP, EPI_SWIGLU_BWD, 128, 0, 0, 1, 1>(ta, tb, p, bound, st, &tc, &td);
   return bn256 ? launch<FPROP, EPI_SWIGLU_BWD, 256, 0, 0, 2>(ta, tb, p, bound, st, &tc, &td)
                : launch<FPROP, EPI_SWIGLU_BWD, 128, 0, 0>(ta, tb, p, bound, st, &tc, &td);
 }

@@ -216,9 +216,9 @@ extern "C" int moe_layer_forward(const moe_layer_config* cfg, const float* logit
   }
   MOE_TRY(moe_permute(x, dest, offsets, counts, w, T, H, E, k, P(P_XP), p_rows, stream));
   MOE_TRY(moe_fc1_swiglu_bf16(P(P_XP), w1, offsets, p_rows, E, L.rmax, H, F, P(P_GU), P(P_H),
-                              stream));
+                              nullptr, stream));
   MOE_TRY(moe_grouped_gemm_bf16(MOE_GEMM_FPROP, P(P_H), w2, 0, offsets, E, L.rmax, 0, H, F,
-                                P(P_Y2), stream));
+                                P(P_Y2), nullptr, nullptr, stream));
   MOE_TRY(moe_unpermute(P(P_Y2), dest, nullptr, T, H, k, out, stream));
   return MOE_OK;
 }
@@ -276,13 +276,13 @@ extern "C" int moe_layer_backward(const moe_layer_config* cfg, const void* dout,
   }
   MOE_TRY(moe_permute(dout, dest, offsets, counts, nullptr, T, H, E, k, P(P_DY2), nullptr, stream));
   MOE_TRY(moe_fc2_dgrad_swiglu_bwd_bf16(P(P_DY2), w2, offsets, p_rows, P(P_GU), E, L.rmax, H, F,
-                                        P(P_DY1), dp, stream));
+                                        P(P_DY1), dp, nullptr, stream));
   MOE_TRY(moe_grouped_gemm_bf16(MOE_GEMM_WGRAD, P(P_H), P(P_DY2), 0, offsets, E, L.rmax, F, H, 0,
-                                dw2, stream));
+                                dw2, nullptr, nullptr, stream));
   MOE_TRY(moe_grouped_gemm_bf16(MOE_GEMM_FPROP, P(P_DY1), w1, 1, offsets, E, L.rmax, 0, H, 2 * F,
-                                P(P_DXP), stream));
+                                P(P_DXP), nullptr, nullptr, stream));
   MOE_TRY(moe_grouped_gemm_bf16(MOE_GEMM_WGRAD, P(P_XP), P(P_DY1), 0, offsets, E, L.rmax, H,
-                                2 * F, 0, dw1, stream));
+                                2 * F, 0, dw1, nullptr, nullptr, stream));
   MOE_TRY(moe_unpermute(P(P_DXP), dest, nullptr, T, H, k, dx, stream));
   MOE_TRY(moe_route_backward(dp, L.parts, L.parts, dest, w, idx, T, E, k, dlogits, stream));
   return MOE_OK;

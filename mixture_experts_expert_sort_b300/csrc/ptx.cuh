@@ -301,6 +301,30 @@ __device__ __forceinline__ void tma_load_2d_cg2(uint32_t dst, const void* tmap, 
       : "memory");
 }
 
+// Row gather: rows r0..r3 of the tensor map (one-row boxes, from column c0)
+// to four consecutive box rows at dst. Rows outside the tensor read the fill
+// value (zeros).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int32_t c0, int32_t r0,
+                                            int32_t r1, int32_t r2, int32_t r3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(bar)
+      : "memory");
+}
+// The same, completing on an mbarrier that may sit in the peer CTA of a pair.
+__device__ __forceinline__ void tma_gather4_cg2(uint32_t dst, const void* tmap, int32_t c0,
+                                                int32_t r0, int32_t r1, int32_t r2, int32_t r3,
+                                                uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(bar)
+      : "memory");
+}
+
 // Tensor-memory allocation for a CTA pair: one warp of each CTA executes it;
 // the same columns are allocated in both CTAs and the address is written to
 // each CTA's dst_smem.

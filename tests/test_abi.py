@@ -97,6 +97,9 @@ def test_layer_workspace_layouts(libmoe):
         assert B.moe_layer_workspace_part(c8, part)[1] == 0, name
     assert B.moe_layer_workspace_part(cb, B.PARTS["x_q_row"][0])[1] == 0
     assert B.moe_layer_workspace_part(c8, B.PARTS["xp"][0])[1] == 0
+    Rb = B.moe_rows_padded_max(T, E, k, 128)  # BF16 rows are not rounded up to 128
+    for name, cols in (("xp", H), ("dy2", H), ("gu", 2 * F)):
+        assert B.moe_layer_workspace_part(cb, B.PARTS[name][0])[1] == Rb * cols * 2, name
     assert B.moe_layer_workspace_size(B.layer_config(64, 384, 256, 4, 2, "mxfp8_act4")) == 0
     assert B.moe_layer_workspace_size(B.layer_config(64, 384, 256, 4, 2, "bf16")) > 0
     assert B.moe_layer_workspace_size(B.layer_config(64, 256, 256, 4, 2, "bf16", align=64)) == 0
@@ -207,6 +210,13 @@ def test_binding_element_types_follow_the_header(host_binding):
     B.moe_grouped_gemm_bf16(B.GEMM_WGRAD, bf(rows, H), bf(rows, F), off)
     B.moe_fc1_swiglu_bf16(bf(rows, H), bf(E, H, 2 * F), off, f32(rows))
     B.moe_fc2_dgrad_swiglu_bwd_bf16(bf(rows, H), bf(E, F, H), off, f32(rows), bf(rows, 2 * F))
+    # row gathers: the gathered operand is the un-permuted [T, .] source
+    B.moe_grouped_gemm_bf16(B.GEMM_FPROP, bf(T, H), bf(E, H, F), off, gather_a=(i32(rows), k))
+    B.moe_grouped_gemm_bf16(B.GEMM_WGRAD, bf(T, H), bf(rows, F), off, gather_a=(i32(rows), k))
+    B.moe_grouped_gemm_bf16(B.GEMM_WGRAD, bf(rows, F), bf(T, H), off, gather_b=(i32(rows), k))
+    B.moe_fc1_swiglu_bf16(bf(T, H), bf(E, H, 2 * F), off, f32(rows), gather_x=(i32(rows), k))
+    B.moe_fc2_dgrad_swiglu_bwd_bf16(bf(T, H), bf(E, F, H), off, f32(rows), bf(rows, 2 * F),
+                                    gather_dy=(i32(rows), k))
     B.moe_grouped_gemm_mxfp8(B.GEMM_FPROP, u8(rows, H), u8(rows * H // 32), u8(F, E * H),
                              u8(F * E * H // 32), off, N=F)
     B.moe_fc1_swiglu_mxfp8(u8(rows, H), u8(rows * H // 32), u8(2 * F, E * H),
@@ -228,6 +238,10 @@ def test_binding_element_types_follow_the_header(host_binding):
         lambda: B.mxfp4_from_mxfp8(i32(rows, H // 4), u8(rows * H // 32)),
         lambda: B.moe_grouped_gemm_bf16(B.GEMM_FPROP, bf(rows, H), bf(E, H, F), off.long()),
         lambda: B.moe_fc1_swiglu_bf16(bf(rows, H), bf(E, H, 2 * F), off, bf(rows)),
+        lambda: B.moe_fc1_swiglu_bf16(bf(T, H), bf(E, H, 2 * F), off, f32(rows),
+                                      gather_x=(i32(rows).long(), k)),  # src is int32
+        lambda: B.moe_layer_backward(cfg, f32(T, H), bf(E, H, 2 * F), bf(E, F, H), bf(T, H),
+                                     bf(E, H, 2 * F), bf(E, F, H), f32(T, E), u8(64)),
         lambda: B.moe_layer_forward(cfg, bf(T, E), bf(T, H), bf(E, H, 2 * F), bf(E, F, H),
                                     bf(T, H), u8(64)),
         lambda: B.moe_layer_forward(cfg, f32(T, E), bf(T, H), bf(E, H, 2 * F), bf(E, F, H),
@@ -249,6 +263,10 @@ def test_bad_arguments_return_arg_error_before_any_cuda_call(libmoe):
     from mixture_experts_expert_sort_b300 import binding as B
     L = B.lib()
     P = 0x100000  # a made-up, 256-byte aligned address: never dereferenced here
+    gather = C.byref(B.RowGather(P, 2, 256))
+    div0 = C.byref(B.RowGather(P, 0, 256))
+    nosrc = C.byref(B.RowGather(None, 2, 256))
+    norows = C.byref(B.RowGather(P, 2, 0))
     cases = {
         "route T < 0": ("moe_route", P, -1, 8, 2, P, P, None),
         "route E = 0": ("moe_route", P, 16, 0, 1, P, P, None),
@@ -278,13 +296,28 @@ def test_bad_arguments_return_arg_error_before_any_cuda_call(libmoe):
         "canonical overlap": ("mxfp8_scales_to_canonical", P, 128, 128, P + 64, None),
         "canonical misaligned": ("mxfp8_scales_to_canonical", P + 2, 128, 128, P + (1 << 20),
                                  None),
-        "gemm_bf16 mode": ("moe_grouped_gemm_bf16", 7, P, P, 0, P, 4, 512, 0, 256, 128, P, None),
+        "gemm_bf16 mode": ("moe_grouped_gemm_bf16", 7, P, P, 0, P, 4, 512, 0, 256, 128, P, None,
+                           None, None),
         "gemm_bf16 b_layout": ("moe_grouped_gemm_bf16", 0, P, P, 3, P, 4, 512, 0, 256, 128, P,
-                               None),
-        "gemm_bf16 E = 0": ("moe_grouped_gemm_bf16", 0, P, P, 0, P, 0, 512, 0, 256, 128, P, None),
-        "fc1_swiglu_bf16 F = 0": ("moe_fc1_swiglu_bf16", P, P, P, P, 4, 512, 128, 0, P, P, None),
+                               None, None, None),
+        "gemm_bf16 E = 0": ("moe_grouped_gemm_bf16", 0, P, P, 0, P, 0, 512, 0, 256, 128, P, None,
+                            None, None),
+        "gemm_bf16 FPROP gathers B": ("moe_grouped_gemm_bf16", 0, P, P, 0, P, 4, 512, 0, 256, 128,
+                                      P, None, gather, None),
+        "gemm_bf16 WGRAD gathers both": ("moe_grouped_gemm_bf16", 1, P, P, 0, P, 4, 512, 128, 256,
+                                         0, P, gather, gather, None),
+        "gemm_bf16 gather src_div = 0": ("moe_grouped_gemm_bf16", 0, P, P, 0, P, 4, 512, 0, 256,
+                                         128, P, div0, None, None),
+        "gemm_bf16 gather no src": ("moe_grouped_gemm_bf16", 1, P, P, 0, P, 4, 512, 128, 256, 0,
+                                    P, nosrc, None, None),
+        "fc1_swiglu_bf16 F = 0": ("moe_fc1_swiglu_bf16", P, P, P, P, 4, 512, 128, 0, P, P, None,
+                                  None),
+        "fc1_swiglu_bf16 gather src_rows = 0": ("moe_fc1_swiglu_bf16", P, P, P, P, 4, 512, 128,
+                                                256, P, P, norows, None),
         "fc2_dgrad_bf16 E = 0": ("moe_fc2_dgrad_swiglu_bwd_bf16", P, P, P, P, P, 0, 512, 128,
-                                 256, P, P, None),
+                                 256, P, P, None, None),
+        "fc2_dgrad_bf16 gather src_div = 0": ("moe_fc2_dgrad_swiglu_bwd_bf16", P, P, P, P, P, 4,
+                                              512, 128, 256, P, P, div0, None),
         "gemm_mxfp8 mode": ("moe_grouped_gemm_mxfp8", 5, P, P, 512, 128, P, P, 256, 512, 0, 0, P,
                             4, 0, 256, 128, P, None),
         "gemm_mxfp8 FPROP N % 128": ("moe_grouped_gemm_mxfp8", 0, P, P, 512, 128, P, P, 256, 512,
