@@ -183,13 +183,24 @@ __device__ __forceinline__ int b_half_row(const MxParams& p, int nt, int h) {
 
 // ---------------------------------------------------------------- epilogue helpers
 
+// max(|a|, |b|, |c|), NaN when any input is NaN (one three-input instruction).
+__device__ __forceinline__ float absmax3(float a, float b, float c) {
+  float d;
+  asm("max.NaN.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // MXFP8 of 32 consecutive values held by one thread: their 32 E4M3 codes in
 // w[0..7] (value 4i + j in byte j of w[i]); returns the E8M0 scale byte.
 __device__ __forceinline__ uint32_t quant32(const float* v, uint32_t* w) {
-  // Non-negative floats order like their bit patterns; Inf and NaN are the largest.
-  uint32_t mbits = 0;
+  // amax as a tree of three-input maxima (depth 4); Inf and NaN give scale 0xFF.
+  float t[11];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) mbits = max(mbits, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+  for (int k = 0; k < 10; ++k) t[k] = absmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+  t[10] = absmax3(v[30], v[31], v[31]);
+  const float u0 = absmax3(t[0], t[1], t[2]), u1 = absmax3(t[3], t[4], t[5]);
+  const float u2 = absmax3(t[6], t[7], t[8]), u3 = absmax3(t[9], t[10], t[10]);
+  const uint32_t mbits = __float_as_uint(absmax3(u0, u1, absmax3(u2, u3, u3))) & 0x7FFFFFFFu;
   const uint32_t sb = mbits < 0x7F800000u ? mx_scale_byte(__uint_as_float(mbits)) : 0xFFu;
   if (sb == 0xFFu) {
 #pragma unroll
@@ -434,10 +445,12 @@ __device__ __forceinline__ bool bwd_chunk(const MxParams& p, const TileInfo& ti,
     const float g = bf16_at(gc, j), u = bf16_at(uc, j);
     const float sg = gemm::sigmoidf_fast(g);
     const float silu = g * sg;
-    dp = fmaf(dg[j], silu * u, dp);
-    const float da = dg[j] * pr;  // dA = dH * p
-    dg[j] = da * u * sg * (1.f + g * (1.f - sg));
-    du[j] = da * silu;
+    const float dh_silu = dg[j] * silu;
+    dp = fmaf(dh_silu, u, dp);          // dL/dp += dH * silu(g) * u
+    du[j] = dh_silu * pr;               // dA * silu(g), dA = dH * p
+    // silu'(g) = s (1 + g (1 - s)) = s + silu (1 - s)
+    const float dsilu = fmaf(-silu, sg, silu) + sg;
+    dg[j] = (dg[j] * pr) * u * dsilu;   // dA * u * silu'(g)
   }
   // dg into columns [0, F), du into [F, 2F), both directions: the column-wise
   // blocks through the transpose, then the row-wise ones; the four code boxes

@@ -21,12 +21,32 @@ constexpr int kQCols = 256;      // tile width; a last tile of 128 columns is al
 constexpr int kQThreads = 256;
 constexpr int kQBand = 32;       // row tiles per band of the tile order
 
-// Largest |value| of 32 bf16 (16 packed words) as bf16 bits; non-negative bf16
-// order like their bit patterns and Inf/NaN are the largest.
-__device__ __forceinline__ uint32_t amax_bf16x32(const uint32_t* w) {
-  uint32_t m = 0;
+// Per half, max(|a|, |b|) of two packed bf16 pairs (NaN when either is NaN);
+// the sign bits of the result are not meaningful.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Per half, the largest |value| of n packed bf16 pairs, as a tree (sign bits
+// cleared: non-negative bf16 order like their bit patterns, and Inf/NaN are
+// the largest).
+template <int N>
+__device__ __forceinline__ uint32_t absmax_pairs(const uint32_t* w) {
+  uint32_t t[N / 2];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+  for (int i = 0; i < N / 2; ++i) t[i] = absmax_bf16x2(w[2 * i], w[2 * i + 1]);
+#pragma unroll
+  for (int n = N / 4; n >= 1; n /= 2)
+#pragma unroll
+    for (int i = 0; i < n; ++i) t[i] = absmax_bf16x2(t[2 * i], t[2 * i + 1]);
+  return t[0] & 0x7FFF7FFFu;
+}
+
+// Largest |value| of 32 bf16 (16 packed words) as bf16 bits.
+__device__ __forceinline__ uint32_t amax_bf16x32(const uint32_t* w) {
+  const uint32_t m = absmax_pairs<16>(w);
   return max(m >> 16, m & 0xFFFFu);
 }
 
@@ -209,9 +229,7 @@ __global__ void __launch_bounds__(kQThreads)
           const int r = 16 * half + i;
           col[i] = tile[r * 128 + 4 * qchunk(c >> 2, r) + (c & 3)];
         }
-        uint32_t m = 0;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) m = __vmaxu2(m, col[i] & 0x7FFF7FFFu);
+        uint32_t m = absmax_pairs<16>(col);
         m = __vmaxu2(m, __shfl_xor_sync(0xffffffffu, m, 1));
         const uint32_t sb0 = scale_of_bf16_amax(m & 0xFFFFu), sb1 = scale_of_bf16_amax(m >> 16);
         uint32_t lo[8], hi[8], o[4];
