@@ -21,8 +21,10 @@
 // under the main loop of the next.
 //
 // Tiles are 128 x BN x 64 (BF16). Expert groups are visited in order; within
-// a group the m-tiles of one n-tile are adjacent, so a weight tile is read
-// from HBM once and the group's activations stay in L2.
+// a group (FPROP) the m-tiles of one n-tile are adjacent, so a weight tile is
+// read from HBM once and the group's activations stay in L2. In WGRAD the
+// tiles along the smaller of M and N run fastest, so the smaller operand of
+// the expert stays in L2 and the larger one is read once.
 //
 // Two problem shapes ("modes"):
 //   FPROP: rows [o_e, o_{e+1}) of A times expert e's B (forward and dgrad).
@@ -153,9 +155,17 @@ __device__ __forceinline__ void decode_tile(const Params& p, const int* prefix, 
     ti.nt = local / mtiles;
     ti.k_iters = p.K / BK;
   } else {
+    // The smaller operand of the expert stays in L2 while the larger streams
+    // through once: n-tiles run fastest when A (M columns) is the larger one.
     const int mtiles = p.M / kTileM;
-    ti.mt = local % mtiles;
-    ti.nt = local / mtiles;
+    if (p.M > p.N) {
+      const int ntiles = p.N / BN;
+      ti.nt = local % ntiles;
+      ti.mt = local / ntiles;
+    } else {
+      ti.mt = local % mtiles;
+      ti.nt = local / mtiles;
+    }
     ti.k_iters = ti.rows / BK;
   }
 }

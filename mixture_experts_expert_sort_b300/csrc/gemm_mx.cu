@@ -167,9 +167,17 @@ __device__ __forceinline__ void decode_tile(const MxParams& p, const int* prefix
     ti.nt = local / mtiles;
     ti.k_iters = p.K / BK;
   } else {
+    // The smaller operand of the expert stays in L2 while the larger streams
+    // through once: n-tiles run fastest when A (M columns) is the larger one.
     const int mtiles = p.M / kTileM;
-    ti.mt = local % mtiles;
-    ti.nt = local / mtiles;
+    if (p.M > p.N) {
+      const int ntiles = (p.N + BN - 1) / BN;
+      ti.nt = local % ntiles;
+      ti.mt = local / ntiles;
+    } else {
+      ti.mt = local % mtiles;
+      ti.nt = local / mtiles;
+    }
     ti.k_iters = ti.rows / BK;
   }
 }
