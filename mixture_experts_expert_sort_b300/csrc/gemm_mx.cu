@@ -215,10 +215,14 @@ __device__ __forceinline__ uint32_t quant32(const float* v, uint32_t* w) {
     for (int i = 0; i < 8; ++i) w[i] = 0x7F7F7F7Fu;
   } else {
     const float inv = mx_inv_scale(sb);
+    const uint64_t inv2 = ptx::f2_pack(inv, inv);
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      w[i] = (uint32_t)cvt_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) |
-             ((uint32_t)cvt_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
+    for (int i = 0; i < 8; ++i) {
+      float a0, a1, a2, a3;  // v * 2^-e, two at a time
+      ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(v[4 * i], v[4 * i + 1]), inv2), a0, a1);
+      ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(v[4 * i + 2], v[4 * i + 3]), inv2), a2, a3);
+      w[i] = (uint32_t)cvt_e4m3x2(a0, a1) | ((uint32_t)cvt_e4m3x2(a2, a3) << 16);
+    }
   }
   return sb;
 }
@@ -362,7 +366,13 @@ __device__ __forceinline__ void fwd_pair(const MxParams& p, const TileInfo& ti, 
     ptx::bulk_commit_group();
   }
 #pragma unroll
-  for (int i = 0; i < 32; ++i) g[i] = g[i] * gemm::sigmoidf_fast(g[i]) * u[i] * pr;  // h
+  for (int i = 0; i < 32; i += 2) {  // h = silu(g) u p, two columns at a time
+    const uint64_t g2 = ptx::f2_pack(g[i], g[i + 1]);
+    const uint64_t s2 = ptx::f2_pack(gemm::sigmoidf_fast(g[i]), gemm::sigmoidf_fast(g[i + 1]));
+    const uint64_t h2 = ptx::f2_mul(ptx::f2_mul(ptx::f2_mul(g2, s2), ptx::f2_pack(u[i], u[i + 1])),
+                                    ptx::f2_pack(pr, pr));
+    ptx::f2_unpack(h2, g[i], g[i + 1]);
+  }
   // H: the column-wise block through the transpose (unless the caller wants
   // no column-wise copy), then the row-wise block.
   const bool cols = p.q_col != nullptr;
@@ -413,7 +423,7 @@ __device__ __forceinline__ bool bwd_chunk(const MxParams& p, const TileInfo& ti,
                                           const CUtensorMap* tm_gu, const CUtensorMap* tm_qr,
                                           const CUtensorMap* tm_qc, uint32_t gu_bar,
                                           uint32_t& gu_phase, bool& gu_pending,
-                                          volatile int* s_abort, float& dp) {
+                                          volatile int* s_abort, uint64_t& dp2) {
   const long long F = p.F;
   const int n = (int)(ord >> 16);
   const int c = (int)((ord >> (4 * i)) & 15);
@@ -446,19 +456,24 @@ __device__ __forceinline__ bool bwd_chunk(const MxParams& p, const TileInfo& ti,
     gu_pending = true;
   }
   float dg[32], du[32];
+  // Two columns at a time in packed fp32 pairs (dp2 keeps the even- and
+  // odd-column partial sums of dL/dp apart).
+  const uint64_t pr2 = ptx::f2_pack(pr, pr);
+  const uint64_t one2 = ptx::f2_pack(1.f, 1.f), neg_one2 = ptx::f2_pack(-1.f, -1.f);
 #pragma unroll
-  for (int j = 0; j < 32; ++j) dg[j] = __uint_as_float(dhv[j]);  // dH for now
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const float g = bf16_at(gc, j), u = bf16_at(uc, j);
-    const float sg = gemm::sigmoidf_fast(g);
-    const float silu = g * sg;
-    const float dh_silu = dg[j] * silu;
-    dp = fmaf(dh_silu, u, dp);          // dL/dp += dH * silu(g) * u
-    du[j] = dh_silu * pr;               // dA * silu(g), dA = dH * p
+  for (int j = 0; j < 32; j += 2) {
+    const float g0 = bf16_at(gc, j), g1 = bf16_at(gc, j + 1);
+    const uint64_t g2 = ptx::f2_pack(g0, g1);
+    const uint64_t u2 = ptx::f2_pack(bf16_at(uc, j), bf16_at(uc, j + 1));
+    const uint64_t dh2 = ptx::f2_pack(__uint_as_float(dhv[j]), __uint_as_float(dhv[j + 1]));
+    const uint64_t s2 = ptx::f2_pack(gemm::sigmoidf_fast(g0), gemm::sigmoidf_fast(g1));
+    const uint64_t silu2 = ptx::f2_mul(g2, s2);
+    const uint64_t dh_silu2 = ptx::f2_mul(dh2, silu2);
+    dp2 = ptx::f2_fma(dh_silu2, u2, dp2);                    // dL/dp += dH silu(g) u
+    ptx::f2_unpack(ptx::f2_mul(dh_silu2, pr2), du[j], du[j + 1]);  // dA silu(g), dA = dH p
     // silu'(g) = s (1 + g (1 - s)) = s + silu (1 - s)
-    const float dsilu = fmaf(-silu, sg, silu) + sg;
-    dg[j] = (dg[j] * pr) * u * dsilu;   // dA * u * silu'(g)
+    const uint64_t dsilu2 = ptx::f2_fma(silu2, ptx::f2_fma(s2, neg_one2, one2), s2);
+    ptx::f2_unpack(ptx::f2_mul(ptx::f2_mul(ptx::f2_mul(dh2, pr2), u2), dsilu2), dg[j], dg[j + 1]);
   }
   // dg into columns [0, F), du into [F, 2F), both directions: the column-wise
   // blocks through the transpose, then the row-wise ones; the four code boxes
@@ -548,7 +563,7 @@ __device__ __forceinline__ void epilogue_tile(const MxParams& p, const TileInfo&
   } else {  // EPI_SWIGLU_BWD: accumulator = dH for F-columns nt*256 + [0, 256)
     const float pr = row_ok ? p.p_rows[grow] : 0.f;
     const int ncol = p.N - ti.nt * BN;
-    float dp = 0.f;
+    uint64_t dp2 = ptx::f2_pack(0.f, 0.f);
     // This warp's chunks (parity h, inside the N tail), four bits each, the
     // one in the shared TMEM region first: it is processed from the drained
     // registers outside the loop, which frees them for the rest.
@@ -557,13 +572,16 @@ __device__ __forceinline__ void epilogue_tile(const MxParams& p, const TileInfo&
     const bool first_shared = n > 0 && (int)(ord & 15) == (odd ? h : 6 + h);
     if (n > 0 && !bwd_chunk(p, ti, ord, 0, first_shared ? sh : nullptr, pr, row_ok, grow, rb,
                             tl_tile, lane, xs, gu_stage, tm_gu, tm_qr, tm_qc, gu_bar, gu_phase,
-                            gu_pending, s_abort, dp))
+                            gu_pending, s_abort, dp2))
       return;
 #pragma unroll 1
     for (int i = 1; i < n; ++i)
       if (!bwd_chunk(p, ti, ord, i, nullptr, pr, row_ok, grow, rb, tl_tile, lane, xs, gu_stage,
-                     tm_gu, tm_qr, tm_qc, gu_bar, gu_phase, gu_pending, s_abort, dp))
+                     tm_gu, tm_qr, tm_qc, gu_bar, gu_phase, gu_pending, s_abort, dp2))
         return;
+    float dp_even, dp_odd;
+    ptx::f2_unpack(dp2, dp_even, dp_odd);
+    const float dp = dp_even + dp_odd;
     // This warp's partial of dL/dp over its chunks; the two warps of a lane
     // quarter write the two halves of the tile's partial (n_part = 2 per tile).
     if (row_ok) p.dp_part[grow * p.n_part + 2 * ti.nt + h] = dp;
