@@ -852,12 +852,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           if (rank == 0)
-            ptx::mbar_arrive(tempty_bar(acc));
+            ptx::mbar_arrive_relaxed(tempty_bar(acc));
           else
-            ptx::mbar_arrive_remote(ptx::mapa_shared(tempty_bar(acc), 0));
+            ptx::mbar_arrive_remote_relaxed(ptx::mapa_shared(tempty_bar(acc), 0));
         }
       } else {
-        ptx::mbar_arrive(tempty_bar(acc));
+        ptx::mbar_arrive_relaxed(tempty_bar(acc));
       }
       if (++acc == 2) {
         acc = 0;

@@ -863,12 +863,12 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE, CG>::kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           if (rank == 0)
-            ptx::mbar_arrive(region_bar(r));
+            ptx::mbar_arrive_relaxed(region_bar(r));
           else
-            ptx::mbar_arrive_remote(ptx::mapa_shared(region_bar(r), 0));
+            ptx::mbar_arrive_remote_relaxed(ptx::mapa_shared(region_bar(r), 0));
         }
       } else {
-        ptx::mbar_arrive(region_bar(r));
+        ptx::mbar_arrive_relaxed(region_bar(r));
       }
     };
     for (int t = unit; t < total_tiles; t += n_units, ++j) {

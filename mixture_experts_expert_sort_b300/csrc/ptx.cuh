@@ -313,6 +313,22 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
                : "memory");
 }
 
+// Arrivals that hand tensor-memory columns back to the MMA thread. The
+// arriving thread has finished its tcgen05.ld reads of those columns
+// (tcgen05.wait::ld, then tcgen05.fence::before_thread_sync), and the MMA
+// thread reads no memory the arriving thread wrote, so the arrive needs no
+// release semantics. A release at cluster scope would first wait until the
+// thread's earlier global stores (its output tiles) are visible to the whole
+// cluster, which delayed the peer CTA's hand-over by about a microsecond per
+// tile.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+
 // TMA load into this CTA's shared memory whose completion is counted on an
 // mbarrier that may sit in the peer CTA (shared::cluster address `bar`).
 __device__ __forceinline__ void tma_load_2d_cg2(uint32_t dst, const void* tmap, int32_t c0,
