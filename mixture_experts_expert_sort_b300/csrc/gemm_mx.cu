@@ -102,7 +102,8 @@ struct Cfg {
   static constexpr int kNumBars = 2 * kStages + 6 + (FUSED ? kEpiWarps : 0);
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
   static constexpr int kPrefixOffset = kMiscOffset + 16;
-  static constexpr int kSmemBytes = kPrefixOffset + (kMaxGroups + 1) * 4;
+  // tile prefix [kMaxGroups + 1] ints, then the group offsets [kMaxGroups + 1]
+  static constexpr int kSmemBytes = kPrefixOffset + 2 * (kMaxGroups + 1) * 4;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;
   static_assert(kSmemAlloc <= 232448, "shared memory budget");
   static_assert(448 + kStages * 12 <= 512, "TMEM budget: scale columns of every stage");
@@ -157,7 +158,9 @@ __device__ __forceinline__ void decode_tile(const MxParams& p, const int* prefix
   while (prefix[e + 1] <= t) ++e;
   e_hint = e;
   const int local = t - prefix[e];
-  const long long o0 = p.offsets[e], o1 = p.offsets[e + 1];
+  // group offsets, copied to shared memory after the tile prefix at start-up
+  const int* offs = prefix + kMaxGroups + 1;
+  const long long o0 = offs[e], o1 = offs[e + 1];
   ti.e = e;
   ti.row0 = o0;
   ti.rows = (int)(o1 - o0);
@@ -649,8 +652,10 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE, CG>::kThreads, 1)
     int acc = 0;
     bool bad = false;
     s_prefix[0] = 0;
+    int* s_offs = s_prefix + kMaxGroups + 1;
+    for (int e = 0; e <= p.E; ++e) s_offs[e] = p.offsets[e];
     for (int e = 0; e < p.E; ++e) {
-      int rows = p.offsets[e + 1] - p.offsets[e];
+      int rows = s_offs[e + 1] - s_offs[e];
       if (rows % BM) bad = true;
       int mt = (MODE == FPROP) ? (rows + kTileM - 1) / kTileM : p.M / kTileM;
       acc += mt * n_tiles;
