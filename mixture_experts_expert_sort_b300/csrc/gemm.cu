@@ -83,6 +83,11 @@ struct Params {
 // buffer (32 x 32 boxes, 2 KB each: FC1 stages g, u and h; the FC2 dgrad
 // receives gate and up and stages dg and du).
 constexpr int kEpiBufBytes = 8192;
+// The plain epilogue stores its bf16 tile through TMA too, as 32 x 32 boxes
+// from two per-warp buffers of 2 KB (one box being written while the other is
+// read). Per-lane stores of 32 different rows cost the L1 one pass per row,
+// time that the main loop's shared-memory operand reads then wait for.
+constexpr int kStoreBufBytes = 4096;
 
 // GATHER: the producer keeps the source row of each gathered operand row of
 // a tile (FPROP, 128) or stage (WGRAD, 64) in shared memory.
@@ -93,7 +98,7 @@ struct Smem {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (CG == 2 || BN != 256) ? 6 : 4;
   static constexpr int kEpiOffset = kStages * kStageBytes;  // 1024-byte aligned
-  static constexpr int kGatherOffset = kEpiOffset + (FUSED ? 4 * kEpiBufBytes : 0);
+  static constexpr int kGatherOffset = kEpiOffset + 4 * (FUSED ? kEpiBufBytes : kStoreBufBytes);
   static constexpr int kBarOffset = kGatherOffset + (GATHER ? BM * 4 : 0);
   // full[S], empty[S], tfull[2], tempty[2], drain, gate/up loads[4]
   static constexpr int kNumBars = 2 * kStages + 5 + (FUSED ? 4 : 0);
@@ -333,10 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
-    if (kFused) {
-      ptx::tma_prefetch_desc(&tmC);
-      ptx::tma_prefetch_desc(&tmD);
-    }
+    ptx::tma_prefetch_desc(&tmC);
+    if (kFused) ptx::tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
     if (kPair) {
@@ -645,7 +648,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int e_hint = 0;
-    uint8_t* ebuf = smem + L::kEpiOffset + (warp - 2) * kEpiBufBytes;  // fused: this warp's boxes
+    // this warp's boxes (fused: the SwiGLU tiles; plain: two store boxes)
+    uint8_t* ebuf = smem + L::kEpiOffset + (warp - 2) * (kFused ? kEpiBufBytes : kStoreBufBytes);
     const uint32_t ebuf_s = ptx::smem_u32(ebuf);
     const uint32_t gu_bar = gu_bar_of(warp - 2);
     uint32_t gu_phase = 0;
@@ -672,9 +676,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tm = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       const bool has_acc = ti.k_iters > 0;
       const int mrow = ti.mt * kTileM + (int)rank * BM + r;  // row of the group's tile rows
+      // Plain epilogue through TMA: chunk c's 32 x 32 box of this warp's rows
+      // (C row crow0) goes out from buffer c & 1.
+      auto store_box = [&](int c, const float* f, long long crow0) {
+        uint8_t* box = ebuf + (c & 1) * 2048;
+        if (lane == 0) ptx::bulk_wait_read_1();  // the box written two chunks ago was read
+        __syncwarp();
+        stage_bf16_row(box, lane, f);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(&tmC, ti.nt * BN + c * 32, (int)crow0, ptx::smem_u32(box));
+          ptx::bulk_commit_group();
+        }
+      };
       if (MODE == WGRAD) {
-        __nv_bfloat16* crow = p.C + (long long)ti.e * p.c_group_stride +
-                              (long long)mrow * p.ldc + (long long)ti.nt * BN;
+        // C viewed as [E * M, N]: this warp's rows start at e * M + its first row
+        const long long crow0 = (long long)ti.e * p.M + (mrow - lane);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
@@ -688,13 +706,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = 0.f;
           }
-          store32_bf16(crow + c * 32, f);
+          store_box(c, f, crow0);
         }
       } else {
         const int lrow = mrow;
         const bool row_ok = lrow < ti.rows;
         const long long grow = ti.row0 + lrow;
         if (EPI == EPI_STORE) {
+          // A warp whose rows straddle the end of a ragged group stores per lane.
           __nv_bfloat16* crow = p.C + grow * p.ldc + (long long)ti.nt * BN;
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
@@ -704,7 +723,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-            if (row_ok) store32_bf16(crow + c * 32, f);
+            if (warp_full)
+              store_box(c, f, rb);
+            else if (row_ok)
+              store32_bf16(crow + c * 32, f);
           }
         } else if (EPI == EPI_SWIGLU_FWD && warp_full) {
           // [g | u] and H leave as 32 x 32 boxes through this warp's buffer
@@ -866,9 +888,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Bulk stores must be complete, and a gate/up load left in flight by an
     // abort must have landed, before this CTA's shared memory goes away.
-    if (kFused && lane == 0) {
+    if (lane == 0) {
       ptx::bulk_wait_all();
-      if (gu_pending) drain_wait(gu_bar, gu_phase);
+      if (kFused && gu_pending) drain_wait(gu_bar, gu_phase);
     }
   }
   ptx::tc_fence_before();
@@ -914,7 +936,7 @@ static int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
                   const CUtensorMap* td = nullptr) {
   auto kern = grouped_gemm_bf16_kernel<MODE, EPI, BN, A_MN, B_MN, CG, G>;
   const int smem = Smem<BN, CG, EPI != EPI_STORE, G != 0>::kAlloc;
-  const CUtensorMap& mc = tc ? *tc : tb;  // the plain epilogue uses neither
+  const CUtensorMap& mc = tc ? *tc : tb;  // plain epilogue: C; fused: see the kernel
   const CUtensorMap& md = td ? *td : tb;
   static bool attr_set = false;
   static int max_units = 0;  // co-resident CTAs (CG = 1) or CTA pairs (CG = 2)
@@ -1031,18 +1053,22 @@ extern "C" int moe_grouped_gemm_bf16(int mode, const void* A, const void* B, int
       return MOE_ERR_CUDA;
     }
     long long bound = (rows / BM + E) * (long long)(N / 128);
+    // C [rows, N], stored by TMA in 32 x 32 boxes
+    CUtensorMap tc;
+    if (!make_tmap(&tc, C, kBF16, 2, rows, N, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return MOE_ERR_CUDA;
     if (ga) {
       if (bn256)
-        return b_layout ? launch<FPROP, EPI_STORE, 256, 0, 0, 2, 1>(ta, tb, p, bound, st)
-                        : launch<FPROP, EPI_STORE, 256, 0, 1, 2, 1>(ta, tb, p, bound, st);
-      return b_layout ? launch<FPROP, EPI_STORE, 128, 0, 0, 1, 1>(ta, tb, p, bound, st)
-                      : launch<FPROP, EPI_STORE, 128, 0, 1, 1, 1>(ta, tb, p, bound, st);
+        return b_layout ? launch<FPROP, EPI_STORE, 256, 0, 0, 2, 1>(ta, tb, p, bound, st, &tc)
+                        : launch<FPROP, EPI_STORE, 256, 0, 1, 2, 1>(ta, tb, p, bound, st, &tc);
+      return b_layout ? launch<FPROP, EPI_STORE, 128, 0, 0, 1, 1>(ta, tb, p, bound, st, &tc)
+                      : launch<FPROP, EPI_STORE, 128, 0, 1, 1, 1>(ta, tb, p, bound, st, &tc);
     }
     if (bn256)
-      return b_layout ? launch<FPROP, EPI_STORE, 256, 0, 0, 2>(ta, tb, p, bound, st)
-                      : launch<FPROP, EPI_STORE, 256, 0, 1, 2>(ta, tb, p, bound, st);
-    return b_layout ? launch<FPROP, EPI_STORE, 128, 0, 0>(ta, tb, p, bound, st)
-                    : launch<FPROP, EPI_STORE, 128, 0, 1>(ta, tb, p, bound, st);
+      return b_layout ? launch<FPROP, EPI_STORE, 256, 0, 0, 2>(ta, tb, p, bound, st, &tc)
+                      : launch<FPROP, EPI_STORE, 256, 0, 1, 2>(ta, tb, p, bound, st, &tc);
+    return b_layout ? launch<FPROP, EPI_STORE, 128, 0, 0>(ta, tb, p, bound, st, &tc)
+                    : launch<FPROP, EPI_STORE, 128, 0, 1>(ta, tb, p, bound, st, &tc);
   }
   if (mode == MOE_GEMM_WGRAD) {
     if (M < BM || M % BM || N < 128 || N % 128) return MOE_ERR_ARG;
@@ -1063,17 +1089,21 @@ extern "C" int moe_grouped_gemm_bf16(int mode, const void* A, const void* B, int
     }
     long long bound = (long long)E * (M / BM) * (N / 128);
     const int g = rows > 0 ? (ga ? 1 : gb ? 2 : 0) : 0;
+    // C viewed as [E * M, N], stored by TMA in 32 x 32 boxes
+    CUtensorMap tc;
+    if (!make_tmap(&tc, C, kBF16, 2, (long long)E * M, N, N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return MOE_ERR_CUDA;
     if (bn256 && M % 256 == 0)
-      return g == 1   ? launch<WGRAD, EPI_STORE, 256, 1, 1, 2, 1>(ta, tb, p, bound, st)
-             : g == 2 ? launch<WGRAD, EPI_STORE, 256, 1, 1, 2, 2>(ta, tb, p, bound, st)
-                      : launch<WGRAD, EPI_STORE, 256, 1, 1, 2>(ta, tb, p, bound, st);
+      return g == 1   ? launch<WGRAD, EPI_STORE, 256, 1, 1, 2, 1>(ta, tb, p, bound, st, &tc)
+             : g == 2 ? launch<WGRAD, EPI_STORE, 256, 1, 1, 2, 2>(ta, tb, p, bound, st, &tc)
+                      : launch<WGRAD, EPI_STORE, 256, 1, 1, 2>(ta, tb, p, bound, st, &tc);
     if (bn256)
-      return g == 1   ? launch<WGRAD, EPI_STORE, 256, 1, 1, 1, 1>(ta, tb, p, bound, st)
-             : g == 2 ? launch<WGRAD, EPI_STORE, 256, 1, 1, 1, 2>(ta, tb, p, bound, st)
-                      : launch<WGRAD, EPI_STORE, 256, 1, 1>(ta, tb, p, bound, st);
-    return g == 1   ? launch<WGRAD, EPI_STORE, 128, 1, 1, 1, 1>(ta, tb, p, bound, st)
-           : g == 2 ? launch<WGRAD, EPI_STORE, 128, 1, 1, 1, 2>(ta, tb, p, bound, st)
-                    : launch<WGRAD, EPI_STORE, 128, 1, 1>(ta, tb, p, bound, st);
+      return g == 1   ? launch<WGRAD, EPI_STORE, 256, 1, 1, 1, 1>(ta, tb, p, bound, st, &tc)
+             : g == 2 ? launch<WGRAD, EPI_STORE, 256, 1, 1, 1, 2>(ta, tb, p, bound, st, &tc)
+                      : launch<WGRAD, EPI_STORE, 256, 1, 1>(ta, tb, p, bound, st, &tc);
+    return g == 1   ? launch<WGRAD, EPI_STORE, 128, 1, 1, 1, 1>(ta, tb, p, bound, st, &tc)
+           : g == 2 ? launch<WGRAD, EPI_STORE, 128, 1, 1, 1, 2>(ta, tb, p, bound, st, &tc)
+                    : launch<WGRAD, EPI_STORE, 128, 1, 1>(ta, tb, p, bound, st, &tc);
   }
   return MOE_ERR_ARG;
 }

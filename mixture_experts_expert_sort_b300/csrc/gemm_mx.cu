@@ -67,6 +67,11 @@ constexpr int kWarpBufBytes = 5120;
 // Per-warp gate/up staging: two 32 x 32 bf16 boxes (64-byte rows, 64-byte
 // swizzle): the backward's TMA loads, the forward's TMA stores.
 constexpr int kGuBytes = 4096;
+// The plain epilogue stores its bf16 tile through TMA as 32 x 32 boxes from
+// two per-warp buffers of 2 KB (one being written while the other is read):
+// per-lane stores of 32 different rows cost the L1 one pass per row, and the
+// main loop's shared-memory operand reads wait for them.
+constexpr int kStoreBufBytes = 4096;
 
 __host__ __device__ constexpr int round1024(int x) { return (x + 1023) / 1024 * 1024; }
 
@@ -96,7 +101,8 @@ struct Cfg {
   // of all stages follow in a region of their own.
   static constexpr int kSfOffset = kStages * kStageBytes;
   static constexpr int kXposeOffset = round1024(kSfOffset + kStages * kSfStageBytes);
-  static constexpr int kGuOffset = kXposeOffset + (FUSED ? kEpiWarps * kWarpBufBytes : 0);
+  static constexpr int kGuOffset =
+      kXposeOffset + kEpiWarps * (FUSED ? kWarpBufBytes : kStoreBufBytes);
   static constexpr int kBarOffset = kGuOffset + (FUSED ? kEpiWarps * kGuBytes : 0);
   // full[S], empty[S], tfull[2], region_empty[3], drain, gate/up loads[epilogue warps]
   static constexpr int kNumBars = 2 * kStages + 6 + (FUSED ? kEpiWarps : 0);
@@ -524,9 +530,24 @@ __device__ __forceinline__ void epilogue_tile(const MxParams& p, const TileInfo&
   // (WGRAD)
   const long long lrow = (long long)rbase + q * 32 + lane;
   const bool has_acc = ti.k_iters > 0;
+  // Plain epilogues: chunk c's 32 x 32 box of this warp's rows (C row crow0 of
+  // the map tm_gu, which is the output's map here) leaves from buffer c & 1.
+  uint8_t* sbuf = reinterpret_cast<uint8_t*>(xs);
+  auto store_box = [&](int c, const float* f, long long crow0) {
+    uint8_t* box = sbuf + (c & 1) * 2048;
+    if (lane == 0) ptx::bulk_wait_read_1();  // the box written two chunks ago was read
+    __syncwarp();
+    gemm::stage_bf16_row(box, lane, f);
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      ptx::tma_store_2d(tm_gu, ti.nt * BN + c * 32, (int)crow0, ptx::smem_u32(box));
+      ptx::bulk_commit_group();
+    }
+  };
   if (MODE == WGRAD) {
-    __nv_bfloat16* crow = p.C + (long long)ti.e * p.c_group_stride + lrow * p.ldc +
-                          (long long)ti.nt * BN;
+    // C viewed as [E * M, N]: this warp's rows start at e * M + its first row
+    const long long crow0 = (long long)ti.e * p.M + (lrow - lane);
 #pragma unroll 1
     for (int c = 0; c < 8; ++c) {
       float f[32];
@@ -536,7 +557,7 @@ __device__ __forceinline__ void epilogue_tile(const MxParams& p, const TileInfo&
 #pragma unroll
         for (int i = 0; i < 32; ++i) f[i] = 0.f;
       }
-      gemm::store32_bf16(crow + c * 32, f);
+      store_box(c, f, crow0);
     }
     return;
   }
@@ -544,13 +565,14 @@ __device__ __forceinline__ void epilogue_tile(const MxParams& p, const TileInfo&
   const long long grow = ti.row0 + lrow;
   const long long rb = ti.row0 + (long long)rbase + q * 32;  // first row of the warp
   if (EPI == EPI_STORE) {
+    // Groups hold whole 128-row blocks here, so a live warp's 32 rows all lie in
+    // its group; the box store clips the N tail and rows past the end of C.
     const int ncol = p.N - ti.nt * BN;
-    __nv_bfloat16* crow = p.C + grow * p.ldc + (long long)ti.nt * BN;
 #pragma unroll 1
     for (int c = 0; c < 8; ++c) {
       float f[32];
       acc_chunk<2>(c, odd, 0, sh, tl_tile, f);
-      if (row_ok && c * 32 < ncol) gemm::store32_bf16(crow + c * 32, f);
+      if (c * 32 < ncol) store_box(c, f, rb);
     }
   } else if (EPI == EPI_SWIGLU_FWD) {
     // Tile-local chunks 0..3 are gate, 4..7 are up, for F-columns n0 .. n0+127;
@@ -672,8 +694,8 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE, CG>::kThreads, 1)
     ptx::tma_prefetch_desc(&tmB);
     ptx::tma_prefetch_desc(&tmSFA);
     ptx::tma_prefetch_desc(&tmSFB);
+    ptx::tma_prefetch_desc(&tmC);
     if (EPI != EPI_STORE) {
-      ptx::tma_prefetch_desc(&tmC);
       ptx::tma_prefetch_desc(&tmQr);
       ptx::tma_prefetch_desc(&tmQc);
     }
@@ -852,7 +874,10 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE, CG>::kThreads, 1)
     const int q = warp & 3;          // TMEM lane quarter this warp may access
     const int h = (warp - 2) >> 2;   // chunk parity (fused: two warps per quarter)
     constexpr int NSH = L::kEpiWarps == 8 ? 1 : 2;  // shared chunks drained per warp
-    float* xs = reinterpret_cast<float*>(smem + L::kXposeOffset + (warp - 2) * kWarpBufBytes);
+    // fused: the transpose and code boxes; plain: the two store boxes
+    float* xs = reinterpret_cast<float*>(
+        smem + L::kXposeOffset +
+        (warp - 2) * (EPI != EPI_STORE ? kWarpBufBytes : kStoreBufBytes));
     uint8_t* gu_stage = smem + L::kGuOffset + (warp - 2) * kGuBytes;
     const uint32_t gu_bar = gu_bar_of(warp - 2);
     uint32_t gu_phase = 0;
@@ -926,9 +951,9 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE, CG>::kThreads, 1)
     }
     // Bulk stores must be complete, and a gate/up load left in flight by an
     // abort must have landed, before this CTA's shared memory goes away.
-    if (EPI != EPI_STORE && lane == 0) {
+    if (lane == 0) {
       ptx::bulk_wait_all();
-      if (gu_pending) gemm::drain_wait(gu_bar, gu_phase);
+      if (EPI != EPI_STORE && gu_pending) gemm::drain_wait(gu_bar, gu_phase);
     }
   }
   ptx::tc_fence_before();
@@ -1084,7 +1109,13 @@ extern "C" int moe_grouped_gemm_mxfp8(int mode, const uint8_t* a, const uint8_t*
   if (!MX::u8_map(&m.a, a, a_rows, a_cols) || !MX::u8_map(&m.b, b, b_rows, b_cols) ||
       !MX::scale_map(&m.sfa, sa, a_rows, a_cols) || !MX::scale_map(&m.sfb, sb, b_rows, b_cols))
     return MOE_ERR_CUDA;
-  m.c = m.qr = m.qc = m.b;  // not used by the plain epilogue
+  // the output, stored by TMA in 32 x 32 boxes: FPROP C [a_rows, N], WGRAD C
+  // viewed as [E * M, N]
+  if (!gemm::make_tmap(&m.c, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                       mode == MOE_GEMM_FPROP ? a_rows : (long long)E * M, N, N, 32, 32,
+                       CU_TENSOR_MAP_SWIZZLE_64B))
+    return MOE_ERR_CUDA;
+  m.qr = m.qc = m.b;  // not used by the plain epilogue
   cudaStream_t st = (cudaStream_t)stream;
   if (mode == MOE_GEMM_FPROP) {
     p.b_row_stride = b_row_stride;
