@@ -1229,7 +1229,7 @@ extern "C" int moe_fc2_dgrad_swiglu_bwd_mxfp8(const uint8_t* dy2q, const uint8_t
       !MX::code_map(&m.qc, dy1q_col, 2LL * F, rows))
     return MOE_ERR_CUDA;
   long long bound = (rows / MX::BM + E) * (long long)((F + MX::BN - 1) / MX::BN);
-  // The SwiGLU-backward epilogue, not the MMA, bounds this kernel: a CTA pair
-  // measured slightly slower than one CTA per tile.
-  return MX::launch<FPROP, EPI_SWIGLU_BWD, 1>(m, p, bound, (cudaStream_t)stream);
+  // CTA pairs: each SM stages half of the B tile, which leaves more of the
+  // shared-memory bandwidth to the epilogue's transposes and staging.
+  return MX::launch<FPROP, EPI_SWIGLU_BWD, 2>(m, p, bound, (cudaStream_t)stream);
 }
