@@ -54,6 +54,68 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float a, float b) {
   return r;
 }
 
+// ------------------------------------------------------------ tile order
+// Order of the tiles of one expert's mtiles x ntiles output grid in a grouped
+// GEMM. Where neither operand of the expert fits in its L2 share, the tiles
+// run in bands of g m-tiles (or g n-tiles): the band's rows of one operand stay
+// in L2 while the other operand streams through once per band, and inside a
+// band the banded index runs fastest, so the tiles in flight together share
+// each k-slice of the streamed operand. The direction that streams fewer bytes
+// wins. Where an operand fits, or where a band would hold fewer than
+// `min_band_tiles` tiles (so that one wave of tiles spans several bands),
+// the whole expert is one band along m (prefer_m) or along n.
+// `band_rows` is the L2 share of the resident band in operand rows of K
+// elements; tile_m / tile_n are the operand rows one tile reads of A / B.
+__device__ __forceinline__ void band_order(int local, int mtiles, int ntiles, int tile_m,
+                                           int tile_n, long long band_rows, bool prefer_m,
+                                           int min_band_tiles, int& mt, int& nt) {
+  const int gm = (int)max(1LL, min(band_rows / tile_m, (long long)mtiles));
+  const int gn = (int)max(1LL, min(band_rows / tile_n, (long long)ntiles));
+  bool band_m = prefer_m;
+  int g = prefer_m ? mtiles : ntiles;
+  if (gm < mtiles || gn < ntiles) {
+    if (gm == mtiles) {
+      band_m = true;
+      g = mtiles;
+    } else if (gn == ntiles) {
+      band_m = false;
+      g = ntiles;
+    } else {
+      // operand rows read from DRAM: the streamed operand once per band, the
+      // banded one once
+      const long long cost_m =
+          (long long)((mtiles + gm - 1) / gm) * ntiles * tile_n + (long long)mtiles * tile_m;
+      const long long cost_n =
+          (long long)((ntiles + gn - 1) / gn) * mtiles * tile_m + (long long)ntiles * tile_n;
+      band_m = cost_m <= cost_n;
+      g = band_m ? gm : gn;
+    }
+    if ((long long)g * (band_m ? ntiles : mtiles) < min_band_tiles) {
+      band_m = prefer_m;
+      g = prefer_m ? mtiles : ntiles;
+    }
+  }
+  if (band_m) {
+    const int per = g * ntiles, b = local / per, r = local - b * per, m0 = b * g;
+    const int gs = min(g, mtiles - m0);
+    mt = m0 + r % gs;
+    nt = r / gs;
+  } else {
+    const int per = g * mtiles, b = local / per, r = local - b * per, n0 = b * g;
+    const int gs = min(g, ntiles - n0);
+    nt = n0 + r % gs;
+    mt = r / gs;
+  }
+}
+
+// L2 share given to the resident band of a grouped GEMM (bytes). The 126 MB
+// L2 also holds the streamed operand's k-slices in flight and the output
+// tiles on their way to memory.
+#ifndef MOE_L2_BAND_MB
+#define MOE_L2_BAND_MB 32
+#endif
+constexpr long long kL2BandBytes = (long long)MOE_L2_BAND_MB << 20;
+
 // Byte offset of the scale for (row r, 32-column block kb) in the tiled
 // scale layout of an operand with K columns (see mxfp8_quantize in moe.h).
 __device__ __forceinline__ long long mx_scale_offset(long long r, long long kb, long long K) {

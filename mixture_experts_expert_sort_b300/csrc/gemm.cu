@@ -75,6 +75,7 @@ struct Params {
   const int32_t* g_src;
   int g_div;
   long long g_n;
+  long long l2_elems;  // L2 share of the resident tile band, in elements
 };
 
 // CG = 2: a CTA pair shares each tile (M = 256), each CTA staging its own 128
@@ -154,25 +155,16 @@ __device__ __forceinline__ void decode_tile(const Params& p, const int* prefix, 
   ti.e = e;
   ti.row0 = o0;
   ti.rows = (int)(o1 - o0);
-  if (MODE == FPROP) {
-    const int mtiles = (ti.rows + kTileM - 1) / kTileM;
-    ti.mt = local % mtiles;
-    ti.nt = local / mtiles;
-    ti.k_iters = p.K / BK;
-  } else {
-    // The smaller operand of the expert stays in L2 while the larger streams
-    // through once: n-tiles run fastest when A (M columns) is the larger one.
-    const int mtiles = p.M / kTileM;
-    if (p.M > p.N) {
-      const int ntiles = p.N / BN;
-      ti.nt = local % ntiles;
-      ti.mt = local / ntiles;
-    } else {
-      ti.mt = local % mtiles;
-      ti.nt = local / mtiles;
-    }
-    ti.k_iters = ti.rows / BK;
-  }
+  const int K = MODE == FPROP ? p.K : ti.rows;
+  const int mtiles = MODE == FPROP ? (ti.rows + kTileM - 1) / kTileM : p.M / kTileM;
+  // an expert's whole grid: m-tiles fastest, except for a weight gradient
+  // whose A (M columns) is the larger operand
+  const bool prefer_m = MODE == FPROP || p.M <= p.N;
+  // bands of at least two waves of tiles
+  const int min_band = 2 * (int)(CG == 2 ? gridDim.x >> 1 : gridDim.x);
+  band_order(local, mtiles, p.N / BN, kTileM, BN, p.l2_elems / max(K, 1), prefer_m, min_band,
+             ti.mt, ti.nt);
+  ti.k_iters = K / BK;
 }
 
 // Global column of B-tile half h (each half is BN/2 columns wide).
@@ -931,9 +923,11 @@ static int num_sms() {
 // tiles_bound: an upper bound on the tiles of the launch (for CG = 2, on the
 // 256-row tiles that CTA pairs take).
 template <int MODE, int EPI, int BN, int A_MN, int B_MN, int CG = 1, int G = 0>
-static int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p,
+static int launch(const CUtensorMap& ta, const CUtensorMap& tb, const Params& p_in,
                   long long tiles_bound, cudaStream_t st, const CUtensorMap* tc = nullptr,
                   const CUtensorMap* td = nullptr) {
+  Params p = p_in;
+  p.l2_elems = kL2BandBytes / 2;
   auto kern = grouped_gemm_bf16_kernel<MODE, EPI, BN, A_MN, B_MN, CG, G>;
   const int smem = Smem<BN, CG, EPI != EPI_STORE, G != 0>::kAlloc;
   const CUtensorMap& mc = tc ? *tc : tb;  // plain epilogue: C; fused: see the kernel

@@ -147,6 +147,7 @@ struct MxParams {
   long long q_col_ld;
   float* dp_part;
   int n_part;
+  long long l2_elems;  // L2 share of the resident tile band, in elements (bytes)
 };
 
 struct TileInfo {
@@ -170,25 +171,16 @@ __device__ __forceinline__ void decode_tile(const MxParams& p, const int* prefix
   ti.e = e;
   ti.row0 = o0;
   ti.rows = (int)(o1 - o0);
-  if (MODE == FPROP) {
-    const int mtiles = (ti.rows + kTileM - 1) / kTileM;
-    ti.mt = local % mtiles;
-    ti.nt = local / mtiles;
-    ti.k_iters = p.K / BK;
-  } else {
-    // The smaller operand of the expert stays in L2 while the larger streams
-    // through once: n-tiles run fastest when A (M columns) is the larger one.
-    const int mtiles = p.M / kTileM;
-    if (p.M > p.N) {
-      const int ntiles = (p.N + BN - 1) / BN;
-      ti.nt = local % ntiles;
-      ti.mt = local / ntiles;
-    } else {
-      ti.mt = local % mtiles;
-      ti.nt = local / mtiles;
-    }
-    ti.k_iters = ti.rows / BK;
-  }
+  const int K = MODE == FPROP ? p.K : ti.rows;
+  const int mtiles = MODE == FPROP ? (ti.rows + kTileM - 1) / kTileM : p.M / kTileM;
+  // an expert's whole grid: m-tiles fastest, except for a weight gradient
+  // whose A (M columns) is the larger operand
+  const bool prefer_m = MODE == FPROP || p.M <= p.N;
+  // bands of at least two waves of tiles
+  const int min_band = 2 * (int)(CG == 2 ? gridDim.x >> 1 : gridDim.x);
+  band_order(local, mtiles, (p.N + BN - 1) / BN, kTileM, BN, p.l2_elems / max(K, 1), prefer_m, min_band,
+             ti.mt, ti.nt);
+  ti.k_iters = K / BK;
 }
 
 // First B row of tile half h (each half is 128 rows of B = 128 output columns).
@@ -981,7 +973,9 @@ struct Maps {
 
 // tiles_bound: an upper bound on the launch's 128-row tiles.
 template <int MODE, int EPI, int CG = 1>
-static int launch(const Maps& m, const MxParams& p, long long tiles_bound, cudaStream_t st) {
+static int launch(const Maps& m, const MxParams& p_in, long long tiles_bound, cudaStream_t st) {
+  MxParams p = p_in;
+  p.l2_elems = kL2BandBytes;  // one-byte elements
   using L = Cfg<EPI != EPI_STORE, CG>;
   auto kern = grouped_gemm_mxf8_kernel<MODE, EPI, CG>;
   static bool attr_set = false;
