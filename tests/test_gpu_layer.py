@@ -1,5 +1,6 @@
 """Whole-layer parity (BF16): the library's forward + backward against the CPU
-oracle's per-expert loop, on the seeded synthetic workloads.
+oracles' per-expert loop (numpy, and at full parity the C++ oracle too), on the
+seeded synthetic workloads.
 
 Integer results (routing indices, counts, offsets, dest, src) must match
 bit-exactly. Float results must have relative Frobenius error <= 5e-3 and
@@ -13,6 +14,7 @@ import pytest
 import torch
 
 from mixture_experts_expert_sort_b300 import inputs as I
+from oracle import cpp_oracle as CO
 from oracle import moe_oracle as O
 from tests.helpers import f64, i32, rel_fro, max_abs_rel
 
@@ -61,6 +63,22 @@ def _full_parity(wl, inp):
     _check("dW1", f64(g["dW1"]), bwd["dW1"])
     _check("dW2", f64(g["dW2"]), bwd["dW2"])
     _check("dlogits", f64(g["dlogits"]), bwd["dlogits"])
+    _check_cpp_oracle(L, wl, inp, g, "bf16")
+
+
+def _check_cpp_oracle(L, wl, inp, g, mode):
+    """The same results against the C++ oracle: its routing and plan bit for
+    bit, the float outputs at the same tolerance."""
+    r = CO.layer(f64(inp["x"]), f64(inp["logits"]), f64(inp["w1"]), f64(inp["w2"]),
+                 f64(inp["dout"]), wl.k, mode)
+    np.testing.assert_array_equal(i32(L.part("idx")).reshape(wl.T, wl.k), r["idx"])
+    counts, offsets, dest, src = CO.permute_plan(r["idx"], wl.E, wl.align)
+    np.testing.assert_array_equal(i32(L.part("counts")), counts)
+    np.testing.assert_array_equal(i32(L.part("offsets")), offsets)
+    np.testing.assert_array_equal(i32(L.part("dest")), dest)
+    np.testing.assert_array_equal(i32(L.part("src"))[:len(src)], src)
+    for n in ("out", "dX", "dW1", "dW2", "dlogits"):
+        _check(n + " (C++ oracle)", f64(g[n]), r[n])
 
 
 def test_tiny_workload_full_parity():

@@ -1,5 +1,6 @@
 """Whole-layer parity (MXFP8): the library's forward + backward against the CPU
-oracle's per-expert loop with MXFP8 emulation, on the seeded workloads.
+oracles' per-expert loop with MXFP8 emulation (numpy, and at full parity the
+C++ oracle too), on the seeded workloads.
 
 Bit-exact: routing indices, the expert-sort plan, and every MXFP8 byte and
 scale the layer computes from inputs that both sides hold identically (x and
@@ -15,6 +16,7 @@ import pytest
 import torch
 
 from mixture_experts_expert_sort_b300 import inputs as I
+from oracle import cpp_oracle as CO
 from oracle import moe_oracle as O
 from tests.helpers import f64, i32, u8, rel_fro, max_abs_rel, scales_tiled_to_rowmajor
 
@@ -66,9 +68,10 @@ def _check_rowwise(L, name, mn, kd, rows, ref_vals):
     sel = torch.as_tensor(rows, device=DEV)
     q = u8(L.part(f"{name}_q_row").view(mn, kd)[sel])
     s = scales_tiled_to_rowmajor(u8(L.part(f"{name}_s_row")), mn, kd)[rows]
-    rq, rs = O.mx_quantize(ref_vals, axis=1)
-    np.testing.assert_array_equal(q, rq, err_msg=f"{name} row-wise codes")
-    np.testing.assert_array_equal(s, rs, err_msg=f"{name} row-wise scales")
+    for quantize in (O.mx_quantize, CO.mx_quantize):  # both oracles
+        rq, rs = quantize(ref_vals, axis=1)
+        np.testing.assert_array_equal(q, rq, err_msg=f"{name} row-wise codes")
+        np.testing.assert_array_equal(s, rs, err_msg=f"{name} row-wise scales")
 
 
 def _check_colwise(L, name, mn, kd, blocks, block_vals):
@@ -77,10 +80,12 @@ def _check_colwise(L, name, mn, kd, blocks, block_vals):
     qd = L.part(f"{name}_q_col").view(kd, mn)
     s = scales_tiled_to_rowmajor(u8(L.part(f"{name}_s_col")), kd, mn)
     for b, vals in zip(blocks, block_vals):
-        rq, rs = O.mx_quantize(vals, axis=0)  # [32, kd], [1, kd]
-        np.testing.assert_array_equal(u8(qd[:, 32 * b:32 * b + 32]).T, rq,
-                                      err_msg=f"{name} column-wise codes, block {b}")
-        np.testing.assert_array_equal(s[:, b], rs[0], err_msg=f"{name} column-wise scales, {b}")
+        for quantize in (O.mx_quantize, CO.mx_quantize):  # both oracles
+            rq, rs = quantize(vals, axis=0)  # [32, kd], [1, kd]
+            np.testing.assert_array_equal(u8(qd[:, 32 * b:32 * b + 32]).T, rq,
+                                          err_msg=f"{name} column-wise codes, block {b}")
+            np.testing.assert_array_equal(s[:, b], rs[0],
+                                          err_msg=f"{name} column-wise scales, {b}")
 
 
 def _check_input_quantisation(L, wl, inp, n_rows=None, n_blocks=None, seed=0, act4=False):
@@ -111,6 +116,21 @@ def _check_input_quantisation(L, wl, inp, n_rows=None, n_blocks=None, seed=0, ac
         blocks = pick(mn // 32, n_blocks)
         _check_colwise(L, name, mn, kd, blocks,
                        [wv[32 * b:32 * b + 32].astype(np.float64) for b in blocks])
+
+
+def _check_cpp_oracle(L, wl, inp, g, mode):
+    """The same results against the C++ oracle: its routing and plan bit for
+    bit, the float outputs at the same tolerance."""
+    r = CO.layer(f64(inp["x"]), f64(inp["logits"]), f64(inp["w1"]), f64(inp["w2"]),
+                 f64(inp["dout"]), wl.k, mode)
+    np.testing.assert_array_equal(i32(L.part("idx")).reshape(wl.T, wl.k), r["idx"])
+    counts, offsets, dest, src = CO.permute_plan(r["idx"], wl.E, wl.align)
+    np.testing.assert_array_equal(i32(L.part("counts")), counts)
+    np.testing.assert_array_equal(i32(L.part("offsets")), offsets)
+    np.testing.assert_array_equal(i32(L.part("dest")), dest)
+    np.testing.assert_array_equal(i32(L.part("src"))[:len(src)], src)
+    for n in ("out", "dX", "dW1", "dW2", "dlogits"):
+        _check(n + " (C++ oracle)", f64(g[n]), r[n])
 
 
 def _check_plan(L, wl, idx_ref):
@@ -153,6 +173,7 @@ def test_mx_layer_full_parity(T, H, F, E, k, zs, ze, of):
     _check("dW1", f64(g["dW1"]), bwd["dW1"])
     _check("dW2", f64(g["dW2"]), bwd["dW2"])
     _check("dlogits", f64(g["dlogits"]), bwd["dlogits"])
+    _check_cpp_oracle(L, wl, inp, g, "mxfp8")
 
 
 def test_mx_layer_deterministic():
@@ -247,6 +268,7 @@ def test_act4_layer_full_parity(T, H, F, E, k, zs, ze, of):
     _check("dW1", f64(g["dW1"]), bwd["dW1"])
     _check("dW2", f64(g["dW2"]), bwd["dW2"])
     _check("dlogits", f64(g["dlogits"]), bwd["dlogits"])
+    _check_cpp_oracle(L, wl, inp, g, "mxfp8_act4")
     # the MXFP4 chain is what the weight gradients saw: the plain MXFP8
     # oracle differs from it by more than the tolerance on dW1
     ref8 = O.layer_backward(O.layer_forward(x, lg, w1, w2, wl.k, mx=True), x, w1, w2, dout)
