@@ -135,3 +135,30 @@ def layer(x, logits, W1, W2, dout, k, mode="bf16", save_bf16=True):
                                _p(r["dW1"]), _p(r["dW2"]), _p(r["dlogits"]), _p(r["dp"]),
                                _p(r["idx"]), _p(r["w"])), "layer")
     return r
+
+
+def router_forward(x, Wr, k):
+    """logits [T, E], idx, w [T, k], and (L, f [E], P [E]) of the aux loss."""
+    x, Wr = _d(x), _d(Wr)
+    T, H = x.shape
+    E = Wr.shape[1]
+    lg = np.empty((T, E))
+    idx = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k))
+    aux = np.empty(1 + 2 * E)
+    _ok(lib().moe_oracle_router_forward(_p(x), _p(Wr), T, H, E, k, _p(lg), _p(idx), _p(w),
+                                        _p(aux)), "router_forward")
+    return {"logits": lg, "idx": idx, "w": w, "aux": float(aux[0]), "f": aux[1:1 + E].copy(),
+            "P": aux[1 + E:].copy()}
+
+
+def router_backward(x, Wr, logits, f, dlogits_route, coeff):
+    """dlogits = dlogits_route + coeff * dAux/dlogits, dx = dlogits Wr^T, dWr = x^T dlogits."""
+    x, Wr, lg, f, dr = _d(x), _d(Wr), _d(logits), _d(f), _d(dlogits_route)
+    T, H = x.shape
+    E = Wr.shape[1]
+    dl, dx, dw = np.empty((T, E)), np.empty((T, H)), np.empty((H, E))
+    _ok(lib().moe_oracle_router_backward(_p(x), _p(Wr), _p(lg), _p(f), _p(dr),
+                                         C.c_double(coeff), T, H, E, _p(dl), _p(dx), _p(dw)),
+        "router_backward")
+    return dl, dx, dw

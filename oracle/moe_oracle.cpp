@@ -471,6 +471,79 @@ int moe_oracle_mx_quantize(const double* a, long long rows, long long cols, int 
   return 0;
 }
 
+// Router projection [MOEBIO Router: a score for every expert per token]:
+// logits [T, E] = x [T, H] Wr [H, E], then top-k routing (idx, w [T, k]), and
+// the load-balancing statistics [MOEBIO "Engineering Challenges of Efficient
+// Training": an auxiliary loss against uneven expert load] in aux [1 + 2E]:
+// aux[0] = L = E sum_e f_e P_e, aux[1 + e] = f_e = the fraction of the T*k
+// routed pairs that go to expert e, aux[1 + E + e] = P_e = the mean over
+// tokens of the softmax probability of expert e over all E logits.
+int moe_oracle_router_forward(const double* x, const double* Wr, int T, int H, int E, int k,
+                              double* logits, int32_t* idx, double* w, double* aux) {
+  if (T < 1 || H < 1 || E < 1 || k < 1 || k > E) return -1;
+  for (int t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e) {
+      double s = 0.0;
+      for (int h = 0; h < H; ++h) s += x[(size_t)t * H + h] * Wr[(size_t)h * E + e];
+      logits[(size_t)t * E + e] = s;
+    }
+  moe_oracle_route(logits, T, E, k, idx, w);
+  double* f = aux + 1;
+  double* P = aux + 1 + E;
+  for (int e = 0; e < E; ++e) f[e] = P[e] = 0.0;
+  for (long i = 0; i < (long)T * k; ++i) f[idx[i]] += 1.0;
+  for (int e = 0; e < E; ++e) f[e] /= (double)T * k;
+  std::vector<double> s((size_t)E);
+  for (int t = 0; t < T; ++t) {
+    const double* l = logits + (size_t)t * E;
+    double m = l[0], z = 0.0;
+    for (int e = 1; e < E; ++e) m = l[e] > m ? l[e] : m;
+    for (int e = 0; e < E; ++e) z += (s[(size_t)e] = std::exp(l[e] - m));
+    for (int e = 0; e < E; ++e) P[e] += s[(size_t)e] / z / T;
+  }
+  aux[0] = 0.0;
+  for (int e = 0; e < E; ++e) aux[0] += f[e] * P[e];
+  aux[0] *= E;
+  return 0;
+}
+
+// Router backward: dlogits = dlogits_route + coeff * dL/dlogits, where
+// dL/dl[t, e] = (E / T) s[t, e] (f_e - sum_i f_i s[t, i]) with the routed
+// fractions f held fixed (the selection has no gradient) and s the softmax
+// over all E logits; then dx = dlogits Wr^T and dWr = x^T dlogits.
+int moe_oracle_router_backward(const double* x, const double* Wr, const double* logits,
+                               const double* f, const double* dlogits_route, double coeff, int T,
+                               int H, int E, double* dlogits, double* dx, double* dWr) {
+  if (T < 1 || H < 1 || E < 1) return -1;
+  std::vector<double> s((size_t)E);
+  for (int t = 0; t < T; ++t) {
+    const double* l = logits + (size_t)t * E;
+    double m = l[0], z = 0.0, c = 0.0;
+    for (int e = 1; e < E; ++e) m = l[e] > m ? l[e] : m;
+    for (int e = 0; e < E; ++e) z += (s[(size_t)e] = std::exp(l[e] - m));
+    for (int e = 0; e < E; ++e) {
+      s[(size_t)e] /= z;
+      c += f[e] * s[(size_t)e];
+    }
+    for (int e = 0; e < E; ++e)
+      dlogits[(size_t)t * E + e] = dlogits_route[(size_t)t * E + e] +
+                                   coeff * ((double)E / T) * s[(size_t)e] * (f[e] - c);
+  }
+  for (int t = 0; t < T; ++t)
+    for (int h = 0; h < H; ++h) {
+      double acc = 0.0;
+      for (int e = 0; e < E; ++e) acc += dlogits[(size_t)t * E + e] * Wr[(size_t)h * E + e];
+      dx[(size_t)t * H + h] = acc;
+    }
+  // dWr[h, e] summed over tokens in ascending order
+  for (long i = 0; i < (long)H * E; ++i) dWr[i] = 0.0;
+  for (int t = 0; t < T; ++t)
+    for (int h = 0; h < H; ++h)
+      for (int e = 0; e < E; ++e)
+        dWr[(size_t)h * E + e] += x[(size_t)t * H + h] * dlogits[(size_t)t * E + e];
+  return 0;
+}
+
 // The whole layer, forward and backward, as the per-expert loop of
 // [EMT §Challenge 1], for the loss L = sum(out * dout).
 // mode: 0 BF16 (exact products), 1 MXFP8, 2 MXFP8 with MXFP4-carried

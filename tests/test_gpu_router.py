@@ -1,5 +1,5 @@
 """Parity of the router projection and the auxiliary load-balancing loss
-(moe_router_forward / moe_router_backward) with the CPU oracle.
+(moe_router_forward / moe_router_backward) with the CPU oracles (numpy and C++).
 
 The logits are fp32 sums over H on the GPU and exact on the CPU, so they are
 compared within the rounding bound of an H-term fp32 sum. The routing decision
@@ -14,6 +14,7 @@ import pytest
 import torch
 
 from mixture_experts_expert_sort_b300 import inputs as I
+from oracle import cpp_oracle as CO
 from oracle import moe_oracle as O
 from tests.helpers import f64, i32, rel_fro, max_abs_rel
 
@@ -71,6 +72,12 @@ def test_router_forward(T, H, E, k):
     assert abs(aux[0] - L) <= 1e-5 * L + E * (~clear).sum() / (T * k), (aux[0], L)
     np.testing.assert_allclose(aux[1 + E:], P, rtol=1e-5, atol=1e-7)
     assert np.abs(aux[1:1 + E] - f).max() <= (~clear).sum() / (T * k) + 1e-7
+    # the C++ oracle: the same exact logits, routing and statistics
+    c = CO.router_forward(xf, wf, k)
+    assert np.all(np.abs(lg - c["logits"]) <= bound)
+    np.testing.assert_array_equal(gidx[clear], c["idx"][clear])
+    assert abs(aux[0] - c["aux"]) <= 1e-5 * c["aux"] + E * (~clear).sum() / (T * k)
+    np.testing.assert_allclose(aux[1 + E:], c["P"], rtol=1e-5, atol=1e-7)
 
 
 @pytest.mark.parametrize("T,H,E,k", CASES)
@@ -95,6 +102,12 @@ def test_router_backward(T, H, E, k):
     dx_ref, dw_ref = O.router_backward(xf, wf, dl_ref)
     dx_ref = dx_ref + f64(dx_in)
     for name, got, r in (("dx", f64(dx), dx_ref), ("dW_r", f64(dw), dw_ref)):
+        assert rel_fro(got, r) <= 5e-3 and max_abs_rel(got, r) <= 1e-2, (name, rel_fro(got, r))
+    # the C++ oracle, from its own forward
+    c = CO.router_forward(xf, wf, k)
+    dlc, dxc, dwc = CO.router_backward(xf, wf, c["logits"], c["f"], f64(dl_route), coeff)
+    assert rel_fro(f64(dl), dlc) <= 1e-5, rel_fro(f64(dl), dlc)
+    for name, got, r in (("dx", f64(dx), dxc + f64(dx_in)), ("dW_r", f64(dw), dwc)):
         assert rel_fro(got, r) <= 5e-3 and max_abs_rel(got, r) <= 1e-2, (name, rel_fro(got, r))
 
 

@@ -11,6 +11,9 @@ as the numpy oracle, against what the pages and the mathematics fix:
   blocks, and hand-worked E2M1 codes;
 * E = 1, k = 1 reducing to a dense SwiGLU MLP, central differences of the
   exact backward, and invariance under a permutation of the tokens;
+* for the router: written-out dot products, an aux loss of exactly 1 under
+  balanced routing, its one-expert closed form, and central differences of
+  the aux loss through the projection;
 * the MXFP8 and MXFP4-activation layers equal to the block-scaled reference
   of tests/test_oracle_mx_directions.py, whose only quantised product is a
   GEMM blocked along its own reduction index;
@@ -160,7 +163,8 @@ def test_cpp_e4m3_rounding_matches_library_conversion():
     blocks[:, 1:] = v.reshape(-1, 31)
     c, s = CO.mx_quantize(blocks, axis=1)
     assert np.all(s == 127)
-    lib = torch.from_numpy(blocks[:, 1:].copy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    lib = torch.from_numpy(blocks[:, 1:].copy()).to(torch.float8_e4m3fn).view(
+        torch.uint8).numpy()
     np.testing.assert_array_equal(c[:, 1:], lib)
 
 
@@ -324,6 +328,98 @@ def test_cpp_layer_agrees_with_numpy_oracle(mode, mx):
     assert np.all(r["dW1"][4] == 0) and np.all(r["dW2"][4] == 0)
 
 
+# ------------------------------------------------------- router and aux loss
+
+def test_cpp_router_logits_brute_force():
+    rng = np.random.default_rng(41)
+    x, Wr = rng.standard_normal((5, 7)), rng.standard_normal((7, 3))
+    ref = np.zeros((5, 3))
+    for t in range(5):
+        for e in range(3):
+            for h in range(7):
+                ref[t, e] += x[t, h] * Wr[h, e]
+    r = CO.router_forward(x, Wr, 2)
+    np.testing.assert_allclose(r["logits"], ref, rtol=1e-13)
+    idx, w = CO.route(ref, 2)
+    np.testing.assert_array_equal(r["idx"], idx)
+
+
+def test_cpp_aux_loss_is_one_when_balanced():
+    # every expert selected by every token (k = E) with equal logits: f = P = 1/E
+    E, T = 4, 16
+    r = CO.router_forward(np.ones((T, 3)), np.zeros((3, E)), E)
+    assert r["aux"] == 1.0
+    np.testing.assert_array_equal(r["f"], np.full(E, 1 / E))
+    np.testing.assert_array_equal(r["P"], np.full(E, 1 / E))
+
+
+def test_cpp_aux_loss_all_on_one_expert_closed_form():
+    # every token picks expert 0 (k = 1) with logit a against 0: L = E * P_0
+    E, T, a = 5, 10, 2.0
+    Wr = np.zeros((1, E))
+    Wr[0, 0] = a
+    r = CO.router_forward(np.ones((T, 1)), Wr, 1)
+    assert abs(r["aux"] - E * np.exp(a) / (np.exp(a) + E - 1)) < 1e-14
+
+
+def test_cpp_router_backward_brute_force():
+    rng = np.random.default_rng(43)
+    T, H, E = 4, 6, 3
+    x, Wr, dl = rng.standard_normal((T, H)), rng.standard_normal((H, E)), rng.standard_normal((T, E))
+    r = CO.router_forward(x, Wr, 2)
+    dlo, dx, dW = CO.router_backward(x, Wr, r["logits"], r["f"], dl, 0.0)
+    np.testing.assert_array_equal(dlo, dl)
+    for t in range(T):
+        for h in range(H):
+            assert abs(dx[t, h] - sum(dl[t, e] * Wr[h, e] for e in range(E))) < 1e-12
+    for h in range(H):
+        for e in range(E):
+            assert abs(dW[h, e] - sum(x[t, h] * dl[t, e] for t in range(T))) < 1e-12
+
+
+def test_cpp_aux_gradient_central_differences():
+    # d aux / d Wr and d aux / d x through the logits; no routing decision is
+    # near a tie, so the routed fractions stay fixed under the steps
+    rng = np.random.default_rng(44)
+    T, H, E, k = 6, 4, 5, 2
+    x, Wr = rng.standard_normal((T, H)), rng.standard_normal((H, E))
+    r = CO.router_forward(x, Wr, k)
+    assert np.min(np.abs(np.diff(np.sort(r["logits"], axis=1), axis=1))) > 1e-3
+    dl, dx, dW = CO.router_backward(x, Wr, r["logits"], r["f"], np.zeros((T, E)), 1.0)
+    np.testing.assert_allclose(dl.sum(axis=1), 0.0, atol=1e-15)
+    eps = 1e-6
+    for arr, grad in ((Wr, dW), (x, dx)):
+        num = np.zeros_like(arr)
+        for pos in itertools.product(*[range(n) for n in arr.shape]):
+            old = arr[pos]
+            arr[pos] = old + eps
+            lp = CO.router_forward(x, Wr, k)["aux"]
+            arr[pos] = old - eps
+            lm = CO.router_forward(x, Wr, k)["aux"]
+            arr[pos] = old
+            num[pos] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(grad, num, rtol=1e-6, atol=1e-10)
+
+
+def test_cpp_router_agrees_with_numpy_oracle():
+    rng = np.random.default_rng(45)
+    T, H, E, k = 200, 48, 16, 4
+    x, Wr, dr = rng.standard_normal((T, H)), rng.standard_normal((H, E)), rng.standard_normal((T, E))
+    r = CO.router_forward(x, Wr, k)
+    lg = O.router_logits(x, Wr)
+    idx, _ = O.route(lg, k)
+    L, f, P = O.aux_load_balance(lg, idx, E)
+    np.testing.assert_array_equal(r["idx"], idx)
+    np.testing.assert_allclose([r["aux"]], [L], rtol=1e-13)
+    np.testing.assert_allclose(r["f"], f, rtol=1e-15)
+    np.testing.assert_allclose(r["P"], P, rtol=1e-13)
+    dl, dx, dW = CO.router_backward(x, Wr, r["logits"], r["f"], dr, 0.03)
+    dl_ref = dr + 0.03 * O.aux_load_balance_grad(lg, f)
+    dx_ref, dW_ref = O.router_backward(x, Wr, dl_ref)
+    for got, ref in ((dl, dl_ref), (dx, dx_ref), (dW, dW_ref)):
+        assert _rel(got, ref) < TOL
+
+
 # ------------------------------------------- planted mistakes must trip a pin
 
 PLANTS = {
@@ -348,6 +444,9 @@ PLANTS = {
                                 "mx"),
     "act4 chain skips FP4": ("Mat row4 = qdq(row8, 1, kE2M1);", "Mat row4 = row8;", "act4"),
     "gate/up read unrounded": ("if (save_bf16) {", "if (false) {", "bf16"),
+    "aux softmax not normalised": ("P[e] += s[(size_t)e] / z / T;", "P[e] += s[(size_t)e] / T;",
+                                   "aux"),
+    "aux gradient sign flipped": ("(f[e] - c)", "(c - f[e])", "aux_fd"),
 }
 
 
@@ -383,6 +482,10 @@ def _pin_fails(pin):
             test_cpp_mx_layer_equals_block_scaled_reference(*CASES[0], "mxfp8_act4")
         elif pin == "bf16":
             test_cpp_bf16_layer_equals_reference(True)
+        elif pin == "aux":
+            test_cpp_aux_loss_is_one_when_balanced()
+        elif pin == "aux_fd":
+            test_cpp_aux_gradient_central_differences()
     except AssertionError:
         return True
     return False
