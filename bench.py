@@ -174,7 +174,19 @@ class Step:
         L = B.lib()
         s = B.stream_handle()
         T, H, F, E, k, R = wl.T, wl.H, wl.F, wl.E, wl.k, self.rmax
-        p = B.ptr
+        # Every tensor of the step is bound once, so each address is checked
+        # and taken once; the calls then pass plain integers.
+        addr, keep = {}, []
+
+        def p(t):
+            if t is None:
+                return None
+            a = addr.get(id(t))
+            if a is None:
+                a = addr[id(t)] = B.ptr(t)
+                keep.append(t)  # the id stays this tensor's while the step holds it
+            return a
+        self._bound = keep
         RC = B.QUANT_ROWWISE | B.QUANT_COLWISE
         npart = self.nparts
         if self.router:
