@@ -12,6 +12,7 @@
 // thread). HBM-bound: 2 bytes read and 1 + 1/32 bytes written per element
 // and direction.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -19,7 +20,6 @@ namespace {
 constexpr int kQRows = 32;
 constexpr int kQCols = 256;      // tile width; a last tile of 128 columns is allowed
 constexpr int kQThreads = 256;
-constexpr int kQBand = 32;       // row tiles per band of the tile order
 
 // Per half, max(|a|, |b|) of two packed bf16 pairs (NaN when either is NaN);
 // the sign bits of the result are not meaningful.
@@ -54,6 +54,17 @@ __device__ __forceinline__ uint32_t scale_of_bf16_amax(uint32_t abits) {
   return abits >= 0x7F80u ? 0xFFu : mx_scale_byte(__uint_as_float(abits << 16));
 }
 
+// E4M3 codes of the four bf16 values in words a, b (low half first), each
+// scaled by the power of two in both halves of inv2 (exact), as one word.
+__device__ __forceinline__ uint32_t codes4(uint32_t a, uint32_t b, uint64_t inv2) {
+  float a0, a1, b0, b1;
+  ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(a << 16),
+                                          __uint_as_float(a & 0xFFFF0000u)), inv2), a0, a1);
+  ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(b << 16),
+                                          __uint_as_float(b & 0xFFFF0000u)), inv2), b0, b1);
+  return (uint32_t)cvt_e4m3x2(a0, a1) | ((uint32_t)cvt_e4m3x2(b0, b1) << 16);
+}
+
 // E4M3 codes of 32 bf16 values (packed pairs in w) with scale byte sb.
 // half: 0 = each word's low element only, 1 = high only, 2 = both (32 values
 // from 16 words). Writes 8 words of codes.
@@ -64,13 +75,9 @@ __device__ __forceinline__ void codes_of(const uint32_t* w, uint32_t sb, uint32_
     return;
   }
   const float inv = mx_inv_scale(sb);
+  const uint64_t inv2 = ptx::f2_pack(inv, inv);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t a = w[2 * i], b = w[2 * i + 1];
-    const uint32_t lo = cvt_e4m3x2(__uint_as_float(a << 16) * inv, __uint_as_float(a & 0xFFFF0000u) * inv);
-    const uint32_t hi = cvt_e4m3x2(__uint_as_float(b << 16) * inv, __uint_as_float(b & 0xFFFF0000u) * inv);
-    out[i] = lo | (hi << 16);
-  }
+  for (int i = 0; i < 8; ++i) out[i] = codes4(w[2 * i], w[2 * i + 1], inv2);
 }
 
 // Shared-memory tile: 32 rows x 256 bf16 (512 bytes per row); 16-byte chunk
@@ -90,13 +97,9 @@ __device__ __forceinline__ void codes_of16(const uint32_t* w, uint32_t sb, uint3
     return;
   }
   const float inv = mx_inv_scale(sb);
+  const uint64_t inv2 = ptx::f2_pack(inv, inv);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t a = w[2 * i], b = w[2 * i + 1];
-    const uint32_t lo = cvt_e4m3x2(__uint_as_float(a << 16) * inv, __uint_as_float(a & 0xFFFF0000u) * inv);
-    const uint32_t hi = cvt_e4m3x2(__uint_as_float(b << 16) * inv, __uint_as_float(b & 0xFFFF0000u) * inv);
-    out[i] = lo | (hi << 16);
-  }
+  for (int i = 0; i < 4; ++i) out[i] = codes4(w[2 * i], w[2 * i + 1], inv2);
 }
 
 constexpr int kQStages = 4;  // tiles in the shared-memory ring
@@ -110,92 +113,98 @@ __device__ __forceinline__ void cp_async_16z(uint32_t dst, const void* src, bool
                : "memory");
 }
 
-// One CTA works through tiles of 32 rows x 256 columns (grid-stride) with a
-// ring of kQStages tiles in shared memory: each thread copies its own 64
+// The tiles of 32 rows x 256 columns are dealt out in work items: an item is
+// a run of `chunk` consecutive row tiles of one 256-column strip, and items
+// are numbered with the strip fastest, so the CTAs in flight cover all the
+// strips of a few row ranges (complete lines of the row-wise output) and each
+// CTA writes runs of chunk x 32 bytes of every column of its strip (the
+// column-wise output). CTA i takes items i, i + gridDim.x, ...; inside an item
+// the next tile is one row tile down, so only the first tile of an item needs
+// an integer division.
+// A ring of kQStages tiles in shared memory: each thread copies its own 64
 // bytes (row rr, 32-column block b) of the tile kQStages-1 steps ahead with
 // cp.async straight into the swizzled layout, so three tiles are in flight
 // per CTA without holding registers. Row pass: thread (rr, b) quantises its
 // block row-wise. Column pass: thread c owns the word column c (columns 2c
 // and 2c+1) and quantises both 32-row column blocks. Amax is taken on packed
 // bf16 halves with an integer max.
+struct QCursor {
+  int item;    // work item (n_items or more: past the end)
+  int rt, ct;  // row tile and column strip of the tile
+  int rt_end;  // end of the item's row tiles
+};
+
 __global__ void __launch_bounds__(kQThreads)
     mxfp8_quant_kernel(const __nv_bfloat16* __restrict__ in, long long rows, int cols,
                        long long ld, const int32_t* __restrict__ src, int src_div, int dirs,
                        uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row,
-                       uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col) {
+                       uint8_t* __restrict__ q_col, uint8_t* __restrict__ s_col, int chunk) {
   extern __shared__ __align__(16) uint32_t qsm[];  // [kQStages][32 rows x 128 words]
   const int tid = threadIdx.x;
   const int rr = tid >> 3, b = tid & 7;  // row pass: row rr, 32-column block b
-  // Tile indices fit in 32 bits (checked on the host); 64-bit division would
-  // cost more than the quantisation itself.
+  // Tile counts fit in 32 bits (checked on the host).
   const int row_tiles = (int)(rows / kQRows);
   const int col_tiles = (cols + kQCols - 1) / kQCols;
-  const int n_tiles = row_tiles * col_tiles;
+  const int n_items = ((row_tiles + chunk - 1) / chunk) * col_tiles;
   const int step = gridDim.x;
-  const int band_tiles = kQBand * col_tiles;
 
-  // Tile order: bands of kQBand row tiles (1024 rows); inside a band the
-  // tiles run down the rows first, then across the columns. The CTAs in
-  // flight then cover a few thousand columns of about a thousand rows, which
-  // keeps the row reads, the row-wise writes and the column-wise writes
-  // (rows of the transposed output) in long contiguous runs.
-  auto tile_rc = [&](int t, int& rt, int& ct) {
-    const int band = t / band_tiles;
-    const int local = t - band * band_tiles;
-    const int rows_in = min(kQBand, row_tiles - band * kQBand);
-    const int lr = local / rows_in;
-    ct = lr;
-    rt = band * kQBand + (local - lr * rows_in);
+  auto start = [&](QCursor& c, int item) {
+    c.item = item;
+    if (item < n_items) {
+      const int ch = item / col_tiles;
+      c.ct = item - ch * col_tiles;
+      c.rt = ch * chunk;
+      c.rt_end = min(c.rt + chunk, row_tiles);
+    }
   };
-  // Input row of this thread for tile t (-1: a zero row).
-  auto src_row = [&](int t) -> long long {
-    int rt, ct;
-    tile_rc(t, rt, ct);
-    const long long r = (long long)rt * kQRows + rr;
+  auto advance = [&](QCursor& c) {
+    if (++c.rt >= c.rt_end) start(c, c.item + step);
+  };
+  // Input row of this thread for the cursor's tile (-1: a zero row).
+  auto src_row = [&](const QCursor& c) -> long long {
+    const long long r = (long long)c.rt * kQRows + rr;
     if (!src) return r;
     const int sv = src[r];
     return sv < 0 ? -1 : (long long)(sv / src_div);
   };
-  // Copy this thread's 64 bytes of tile t (input row in_row) into ring slot s.
-  auto issue = [&](int t, long long in_row, int s) {
-    int rt, ct;
-    tile_rc(t, rt, ct);
-    const int c = ct * kQCols + 32 * b;
-    const bool ok = in_row >= 0 && c < cols;
-    const __nv_bfloat16* g = ok ? in + in_row * ld + c : in;
+  // Copy this thread's 64 bytes of the cursor's tile (input row in_row) into ring slot s.
+  auto issue = [&](const QCursor& c, long long in_row, int s) {
+    const int col = c.ct * kQCols + 32 * b;
+    const bool ok = in_row >= 0 && col < cols;
+    const __nv_bfloat16* g = ok ? in + in_row * ld + col : in;
     const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(qsm + s * kQTileWords + rr * 128));
 #pragma unroll
     for (int q = 0; q < 4; ++q) cp_async_16z(base + 16 * qchunk(4 * b + q, rr), g + 8 * q, ok);
   };
 
-  // Prologue: tiles 0 .. kQStages-2 of this CTA, and the row index of the next.
-  const int t0 = blockIdx.x;
-  long long row_ahead = 0;  // input row of the tile kQStages-1 steps ahead
+  // Prologue: the first kQStages-1 tiles of this CTA, and the row index of the next.
+  QCursor cur, ahead;
+  start(cur, blockIdx.x);
+  ahead = cur;
 #pragma unroll
   for (int s = 0; s < kQStages - 1; ++s) {
-    const int ts = t0 + s * step;
-    if (ts < n_tiles) issue(ts, src_row(ts), s);
+    if (ahead.item < n_items) {
+      issue(ahead, src_row(ahead), s);
+      advance(ahead);
+    }
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
-  if ((long long)t0 + (kQStages - 1) * (long long)step < n_tiles)
-    row_ahead = src_row(t0 + (kQStages - 1) * step);
+  long long row_ahead = ahead.item < n_items ? src_row(ahead) : 0;
 
   int slot = 0;
-  for (int t = t0; t < n_tiles; t += step) {
+  while (cur.item < n_items) {
     // Issue the tile kQStages-1 steps ahead into the slot freed last iteration.
-    const long long ta = (long long)t + (kQStages - 1) * (long long)step;
-    if (ta < n_tiles) {
-      issue((int)ta, row_ahead, (slot + kQStages - 1) % kQStages);
-      if (ta + step < n_tiles) row_ahead = src_row((int)(ta + step));
+    if (ahead.item < n_items) {
+      issue(ahead, row_ahead, (slot + kQStages - 1) % kQStages);
+      advance(ahead);
+      if (ahead.item < n_items) row_ahead = src_row(ahead);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
     asm volatile("cp.async.wait_group %0;" ::"n"(kQStages - 1) : "memory");
-    __syncthreads();  // tile t is complete in slot `slot` for all threads
+    __syncthreads();  // tile `cur` is complete in slot `slot` for all threads
     const uint32_t* tile = qsm + slot * kQTileWords;
-    int rt, ct;
-    tile_rc(t, rt, ct);
-    const long long r0 = (long long)rt * kQRows;
-    const int c0 = ct * kQCols;
+    const long long r0 = (long long)cur.rt * kQRows;
+    const int c0 = cur.ct * kQCols;
     const int ncol = min(kQCols, cols - c0);  // 256, or 128 for a last half tile
     if ((dirs & MOE_QUANT_ROWWISE) && 32 * b < ncol) {
       uint32_t w[16];
@@ -252,6 +261,7 @@ __global__ void __launch_bounds__(kQThreads)
     }
     __syncthreads();  // slot is reused by the copies issued next iteration
     slot = (slot + 1) % kQStages;
+    advance(cur);
   }
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
@@ -307,9 +317,17 @@ extern "C" int mxfp8_quantize(const void* in, long long rows, int cols, long lon
   if (!in || !aligned16(in)) return MOE_ERR_ARG;
   if ((dirs & MOE_QUANT_ROWWISE) && (!q_row || !s_row || !aligned16(q_row))) return MOE_ERR_ARG;
   if ((dirs & MOE_QUANT_COLWISE) && (!q_col || !s_col || !aligned16(q_col))) return MOE_ERR_ARG;
-  long long tiles = (rows / kQRows) * ((cols + kQCols - 1) / kQCols);
+  const long long row_tiles = rows / kQRows, col_tiles = (cols + kQCols - 1) / kQCols;
+  const long long tiles = row_tiles * col_tiles;
   if (tiles >= (1LL << 31) - 148LL * 3 * 4) return MOE_ERR_UNSUPPORTED;
-  long long blocks = tiles < 148 * 3 ? tiles : 148 * 3;  // 3 CTAs (192 KB of ring) per SM
+  const long long ctas = 148 * 3;  // 3 CTAs (192 KB of ring) per SM
+  // Row tiles per work item: up to 8 (a 256-byte run of each column-wise
+  // output row), and about 32 items per CTA or more, so that the CTAs left
+  // with one item more than the others idle the rest for 3% of the time at most.
+  long long chunk = tiles / (32 * ctas);
+  chunk = chunk < 1 ? 1 : chunk > 8 ? 8 : chunk;
+  const long long items = ((row_tiles + chunk - 1) / chunk) * col_tiles;
+  long long blocks = items < ctas ? items : ctas;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(mxfp8_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -319,6 +337,6 @@ extern "C" int mxfp8_quantize(const void* in, long long rows, int cols, long lon
   }
   mxfp8_quant_kernel<<<(unsigned)blocks, kQThreads, kQSmemBytes, (cudaStream_t)stream>>>(
       static_cast<const __nv_bfloat16*>(in), rows, cols, ld, src, src_div, dirs, q_row, s_row,
-      q_col, s_col);
+      q_col, s_col, (int)chunk);
   return launch_status();
 }
