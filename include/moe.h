@@ -75,6 +75,22 @@ MOE_API int moe_device_error(moe_stream_t stream, unsigned* flags);
  * following moe_device_error reports the bit. Nothing else is touched. */
 MOE_API int moe_selftest_wait_timeout(moe_stream_t stream);
 
+/* moe_selftest_tile_order: a host-side diagnostic of the grouped GEMMs' tile
+ * scheduler; no GPU work. For one expert's grid of mtiles x ntiles output
+ * tiles, writes the m-tile and n-tile that the kernels process as the expert's
+ * local tile t (0 <= t < mtiles * ntiles) into mt[t] and nt[t] (host arrays).
+ * The kernels run an expert's tiles in bands when neither operand fits in its
+ * L2 share: band_rows is that share in operand rows of K elements, tile_m and
+ * tile_n the operand rows one tile reads of A and of B, prefer_m the order of
+ * an expert that is not banded (m-tiles fastest when non-zero), and
+ * min_band_tiles the smallest band (the kernels pass two waves of tiles).
+ * The grouped GEMMs pass band_rows = (32 MiB / element bytes) / K.
+ * Returns MOE_ERR_ARG for non-positive sizes, a negative band_rows, null
+ * arrays or a grid of 2^31 tiles or more. */
+MOE_API int moe_selftest_tile_order(int mtiles, int ntiles, int tile_m, int tile_n,
+                                    long long band_rows, int prefer_m, int min_band_tiles,
+                                    int32_t* mt, int32_t* nt);
+
 /* ------------------------------------------------------------------------
  * Routing. "How MoE Architecture Cuts Costs and Boosts Efficiency: Efficient
  * Training of Biological Foundation Models", the Router paragraph (top-K

@@ -41,6 +41,7 @@ SIGNATURES = {
     "moe_status_string": (C.c_char_p, [_i]),
     "moe_device_error": (_i, [_p, C.POINTER(_u)]),
     "moe_selftest_wait_timeout": (_i, [_p]),
+    "moe_selftest_tile_order": (_i, [_i, _i, _i, _i, _ll, _i, _i, _p, _p]),
     "moe_route": (_i, [_p, _i, _i, _i, _p, _p, _p]),
     "moe_route_backward": (_i, [_p, _ll, _i, _p, _p, _p, _i, _i, _i, _p, _p]),
     "moe_rows_padded_max": (_ll, [_i, _i, _i, _i]),
@@ -157,6 +158,19 @@ def selftest_wait_timeout(stream=None):
     """Run the library's bounded-wait self-test (about 2 s on the device); the
     timeout bit then shows in device_error()."""
     _check(lib().moe_selftest_wait_timeout(stream_handle(stream)), "moe_selftest_wait_timeout")
+
+
+def selftest_tile_order(mtiles, ntiles, tile_m, tile_n, band_rows, prefer_m, min_band_tiles):
+    """Host-side: the (m-tile, n-tile) the grouped GEMMs process as each local
+    tile index of one expert's grid, as two int32 numpy arrays."""
+    import numpy as np
+    mt = np.empty(mtiles * ntiles, dtype=np.int32)
+    nt = np.empty(mtiles * ntiles, dtype=np.int32)
+    _check(lib().moe_selftest_tile_order(mtiles, ntiles, tile_m, tile_n, band_rows,
+                                         int(bool(prefer_m)), min_band_tiles,
+                                         mt.ctypes.data, nt.ctypes.data),
+           "moe_selftest_tile_order")
+    return mt, nt
 
 
 # ----------------------------------------------------------------- routing

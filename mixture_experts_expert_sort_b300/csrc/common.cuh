@@ -66,11 +66,16 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float a, float b) {
 // the whole expert is one band along m (prefer_m) or along n.
 // `band_rows` is the L2 share of the resident band in operand rows of K
 // elements; tile_m / tile_n are the operand rows one tile reads of A / B.
-__device__ __forceinline__ void band_order(int local, int mtiles, int ntiles, int tile_m,
-                                           int tile_n, long long band_rows, bool prefer_m,
-                                           int min_band_tiles, int& mt, int& nt) {
-  const int gm = (int)max(1LL, min(band_rows / tile_m, (long long)mtiles));
-  const int gn = (int)max(1LL, min(band_rows / tile_n, (long long)ntiles));
+__host__ __device__ __forceinline__ int band_size(long long band_rows, int tile, int tiles) {
+  const long long g = band_rows / tile;
+  return g < 1 ? 1 : g > tiles ? tiles : (int)g;
+}
+
+__host__ __device__ __forceinline__ void band_order(int local, int mtiles, int ntiles, int tile_m,
+                                                    int tile_n, long long band_rows, bool prefer_m,
+                                                    int min_band_tiles, int& mt, int& nt) {
+  const int gm = band_size(band_rows, tile_m, mtiles);
+  const int gn = band_size(band_rows, tile_n, ntiles);
   bool band_m = prefer_m;
   int g = prefer_m ? mtiles : ntiles;
   if (gm < mtiles || gn < ntiles) {
@@ -97,12 +102,12 @@ __device__ __forceinline__ void band_order(int local, int mtiles, int ntiles, in
   }
   if (band_m) {
     const int per = g * ntiles, b = local / per, r = local - b * per, m0 = b * g;
-    const int gs = min(g, mtiles - m0);
+    const int gs = g < mtiles - m0 ? g : mtiles - m0;
     mt = m0 + r % gs;
     nt = r / gs;
   } else {
     const int per = g * mtiles, b = local / per, r = local - b * per, n0 = b * g;
-    const int gs = min(g, ntiles - n0);
+    const int gs = g < ntiles - n0 ? g : ntiles - n0;
     nt = n0 + r % gs;
     mt = r / gs;
   }

@@ -32,3 +32,21 @@ extern "C" int moe_selftest_wait_timeout(moe_stream_t stream) {
   moe::selftest_wait_timeout_kernel<<<1, 64, 0, (cudaStream_t)stream>>>();
   return moe::launch_status();
 }
+
+// Host-side check of the grouped GEMMs' tile order: the (m-tile, n-tile) that
+// the kernels' band_order gives each local tile index of one expert's grid.
+extern "C" int moe_selftest_tile_order(int mtiles, int ntiles, int tile_m, int tile_n,
+                                       long long band_rows, int prefer_m, int min_band_tiles,
+                                       int32_t* mt, int32_t* nt) {
+  if (mtiles < 1 || ntiles < 1 || tile_m < 1 || tile_n < 1 || band_rows < 0 || !mt || !nt ||
+      (long long)mtiles * ntiles >= (1LL << 31))
+    return MOE_ERR_ARG;
+  for (int t = 0; t < mtiles * ntiles; ++t) {
+    int m, n;
+    moe::band_order(t, mtiles, ntiles, tile_m, tile_n, band_rows, prefer_m != 0, min_band_tiles,
+                    m, n);
+    mt[t] = m;
+    nt[t] = n;
+  }
+  return MOE_OK;
+}
