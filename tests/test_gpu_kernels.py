@@ -148,6 +148,38 @@ def test_mxfp8_scales_to_canonical(rows, cols):
                                   s_col.T)
 
 
+def test_mxfp8_quantize_large_ragged_work_items():
+    """A matrix large enough that every CTA takes work items of several row
+    tiles (85,376 x 4,224: items of 3 row tiles, the last item of each strip
+    one tile short, and a last strip 128 columns wide), bit-exact against both
+    oracles' quantisers on sampled rows and 32-row blocks, the last ones included."""
+    from oracle import cpp_oracle as CO
+    rows, cols = 85376, 4224
+    g = torch.Generator(device=DEV).manual_seed(21)
+    x = (torch.randn((rows, cols), generator=g, device=DEV) *
+         torch.exp2(torch.randint(-12, 12, (rows, 1), generator=g, device=DEV).float()))
+    x = x.to(torch.bfloat16)
+    q = B().mxfp8_quantize(x)
+    rng = np.random.default_rng(21)
+    pick_rows = np.unique(np.concatenate([[0, 1, rows - 1, rows - 32, rows - 96],
+                                          rng.choice(rows, 40, replace=False)]))
+    xr = f64(x[torch.as_tensor(pick_rows, device=DEV)])
+    s_row = scales_tiled_to_rowmajor(u8(q["s_row"]), rows, cols)
+    s_col = scales_tiled_to_rowmajor(u8(q["s_col"]), cols, rows)
+    for quantize in (O.mx_quantize, CO.mx_quantize):
+        c, s = quantize(xr, axis=1)
+        np.testing.assert_array_equal(u8(q["q_row"][torch.as_tensor(pick_rows, device=DEV)]), c)
+        np.testing.assert_array_equal(s_row[pick_rows], s)
+    blocks = np.unique(np.concatenate([[0, rows // 32 - 1, rows // 32 - 3],
+                                       rng.choice(rows // 32, 12, replace=False)]))
+    for b in blocks:
+        xb = f64(x[32 * b:32 * b + 32])
+        for quantize in (O.mx_quantize, CO.mx_quantize):
+            c, s = quantize(xb, axis=0)
+            np.testing.assert_array_equal(u8(q["q_col"][:, 32 * b:32 * b + 32]).T, c)
+            np.testing.assert_array_equal(s_col[:, b], s[0])
+
+
 def test_mxfp8_quantize_nonfinite_block():
     x = _quant_input(128, 128, 3, special=False)
     x[2, 40] = float("inf")
