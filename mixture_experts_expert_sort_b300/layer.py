@@ -54,6 +54,30 @@ class MoELayer:
         return B.moe_layer_backward(self.cfg, dout, w1, w2, dx, dw1, dw2, dlogits, self.workspace,
                                     stream)
 
+    def capture(self, logits, x, w1, w2, dout, out, dx, dw1, dw2, dlogits):
+        """Record one forward + backward over these fixed device buffers as a
+        CUDA graph and return it (a torch.cuda.CUDAGraph): each replay() runs the
+        layer's launches again on the current stream, reading the buffers' data
+        as it is at replay time, with no host work per launch. The layer runs
+        once on the capture stream first, so every kernel's one-time launch
+        set-up happens outside the capture."""
+        self._expect(logits=logits, x=x, w1=w1, w2=w2, out=out, dout=dout, dx=dx, dw1=dw1,
+                     dw2=dw2, dlogits=dlogits)
+        cs = torch.cuda.Stream(device=self.device)
+        cs.wait_stream(torch.cuda.current_stream(self.device))
+
+        def step():
+            self.forward(logits, x, w1, w2, out=out, stream=cs)
+            self.backward(dout, w1, w2, dx=dx, dw1=dw1, dw2=dw2, dlogits=dlogits, stream=cs)
+
+        with torch.cuda.stream(cs):
+            step()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cs):
+            step()
+        torch.cuda.current_stream(self.device).wait_stream(cs)
+        return graph
+
     def part(self, name):
         """A typed view of one saved intermediate in the workspace."""
         pid, dtype = B.PARTS[name]
