@@ -727,8 +727,9 @@ def e2e_measure(args, step, t, world):
     copies its inputs from pinned host memory and reads its results back, as a
     training loop does; the copies of one step overlap the compute of its
     neighbours (two slots of device buffers, an input-copy stream and a
-    result-copy stream ordered by events), and the compute stays on the
-    launching stream. dW stays resident, as in training."""
+    result-copy stream ordered by events), dOut is copied in while the
+    forward runs and out is read back while the backward runs, and the
+    compute stays on the launching stream. dW stays resident, as in training."""
     layer = step.layer
     x, logits, dout, out, dx, dlogits = t["x"], t["logits"], t["dout"], t["out"], t["dx"], \
         t["dlogits"]
@@ -745,7 +746,7 @@ def e2e_measure(args, step, t, world):
               "dx": torch.empty_like(dx), "dl": torch.empty_like(dlogits)} for _ in range(2)]
     comp = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev = [{"in": torch.cuda.Event(), "comp": torch.cuda.Event(), "out": torch.cuda.Event()}
+    ev = [{k: torch.cuda.Event() for k in ("in_fwd", "in", "fwd", "comp", "out")}
           for _ in range(2)]
     e2e_steps = max(2, min(args.steps, 10))
 
@@ -755,19 +756,26 @@ def e2e_measure(args, step, t, world):
             with torch.cuda.stream(s_in):
                 if i >= 2:
                     s_in.wait_event(e["comp"])  # step i-2 is done with these inputs
-                sl["x"].copy_(h_x, non_blocking=True)
+                # the forward's inputs first; dOut's copy then overlaps the forward
                 sl["lg"].copy_(h_lg, non_blocking=True)
+                sl["x"].copy_(h_x, non_blocking=True)
+                e["in_fwd"].record(s_in)
                 sl["do"].copy_(h_do, non_blocking=True)
                 e["in"].record(s_in)
-            comp.wait_event(e["in"])
+            comp.wait_event(e["in_fwd"])
             if i >= 2:
                 comp.wait_event(e["out"])  # step i-2's results have been read back
             layer.forward(sl["lg"], sl["x"], w1, w2, out=sl["out"])
+            e["fwd"].record(comp)
+            with torch.cuda.stream(s_out):
+                # out is read back while the backward runs
+                s_out.wait_event(e["fwd"])
+                h_out.copy_(sl["out"], non_blocking=True)
+            comp.wait_event(e["in"])
             layer.backward(sl["do"], w1, w2, dx=sl["dx"], dw1=dw1, dw2=dw2, dlogits=sl["dl"])
             e["comp"].record(comp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(e["comp"])
-                h_out.copy_(sl["out"], non_blocking=True)
                 h_dx.copy_(sl["dx"], non_blocking=True)
                 h_dl.copy_(sl["dl"], non_blocking=True)
                 e["out"].record(s_out)
