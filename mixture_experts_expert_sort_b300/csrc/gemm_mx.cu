@@ -88,9 +88,20 @@ __host__ __device__ constexpr int round1024(int x) { return (x + 1023) / 1024 * 
 // the tile's B rows (each SM's tensor core reads the scales of every column
 // of B it multiplies from its own tensor memory). The stage bytes freed go to
 // a deeper ring.
-template <bool FUSED, int CG = 1>
+//
+// The ring's depth sets how much of the operand round trip (a stage's TMA
+// load after the stage is freed) the tensor work in flight covers: copies of
+// the plain pair kernel took 1.15, 1.19 and 1.36 ms with 5, 4 and 3 stages on
+// one Mixtral-shape GEMM. The FC1 epilogue therefore stages its gate/up boxes
+// in its transpose buffer instead of a buffer of their own, which leaves room
+// for a fifth stage; the FC2-dgrad epilogue loads the next chunk's gate/up
+// boxes while it transposes, so it keeps both buffers and four stages.
+template <int EPI, int CG = 1>
 struct Cfg {
-  static constexpr int kStages = FUSED ? (CG == 2 ? 4 : 3) : (CG == 2 ? 5 : 4);
+  static constexpr bool FUSED = EPI != EPI_STORE;
+  static constexpr bool kGuBuf = EPI == EPI_SWIGLU_BWD;  // gate/up boxes need their own buffer
+  static constexpr int kStages =
+      FUSED ? (CG == 2 ? (kGuBuf ? 4 : 5) : 3) : (CG == 2 ? 5 : 4);
   static constexpr int kBBytes = (BN / CG) * BK;  // this CTA's B rows per stage
   static constexpr int kStageBytes = kABytes + kBBytes;
   // bytes of one stage counted on the leader's full barrier (both CTAs of a pair)
@@ -103,7 +114,7 @@ struct Cfg {
   static constexpr int kXposeOffset = round1024(kSfOffset + kStages * kSfStageBytes);
   static constexpr int kGuOffset =
       kXposeOffset + kEpiWarps * (FUSED ? kWarpBufBytes : kStoreBufBytes);
-  static constexpr int kBarOffset = kGuOffset + (FUSED ? kEpiWarps * kGuBytes : 0);
+  static constexpr int kBarOffset = kGuOffset + (kGuBuf ? kEpiWarps * kGuBytes : 0);
   // full[S], empty[S], tfull[2], region_empty[3], drain, gate/up loads[epilogue warps]
   static constexpr int kNumBars = 2 * kStages + 6 + (FUSED ? kEpiWarps : 0);
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
@@ -378,6 +389,9 @@ __device__ __forceinline__ void fwd_pair(const MxParams& p, const TileInfo& ti, 
   // no column-wise copy), then the row-wise block.
   const bool cols = p.q_col != nullptr;
   uint32_t wc[8], wr[8];
+  // the gate/up boxes sit in the same buffer: their TMA stores must have read them
+  if (lane == 0) ptx::bulk_wait_read_all();
+  __syncwarp();
   if (cols) quant_col32(g, wc, p.s_col, p.q_col_ld, col, rb, xs, lane);
   const uint32_t sb = quant32(g, wr);
   if (row_ok) p.s_row[mx_scale_offset(grow, col >> 5, p.q_row_ld)] = (uint8_t)sb;
@@ -606,7 +620,7 @@ __device__ __forceinline__ void epilogue_tile(const MxParams& p, const TileInfo&
 }
 
 template <int MODE, int EPI, int CG>
-__global__ void __launch_bounds__(Cfg<EPI != EPI_STORE, CG>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<EPI, CG>::kThreads, 1)
     grouped_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmSFA,
@@ -614,7 +628,7 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE, CG>::kThreads, 1)
                              const __grid_constant__ CUtensorMap tmC,
                              const __grid_constant__ CUtensorMap tmQr,
                              const __grid_constant__ CUtensorMap tmQc, const MxParams p) {
-  using L = Cfg<EPI != EPI_STORE, CG>;
+  using L = Cfg<EPI, CG>;
   constexpr bool kPair = CG == 2;
   constexpr int kTileM = BM * CG;
   constexpr int kStageBytes = L::kStageBytes;
@@ -870,7 +884,10 @@ __global__ void __launch_bounds__(Cfg<EPI != EPI_STORE, CG>::kThreads, 1)
     float* xs = reinterpret_cast<float*>(
         smem + L::kXposeOffset +
         (warp - 2) * (EPI != EPI_STORE ? kWarpBufBytes : kStoreBufBytes));
-    uint8_t* gu_stage = smem + L::kGuOffset + (warp - 2) * kGuBytes;
+    // FC2 dgrad: the gate/up loads' own buffer; FC1: the transpose buffer
+    // (its gate/up boxes are stored before the transpose reuses it)
+    uint8_t* gu_stage = L::kGuBuf ? smem + L::kGuOffset + (warp - 2) * kGuBytes
+                                  : reinterpret_cast<uint8_t*>(xs);
     const uint32_t gu_bar = gu_bar_of(warp - 2);
     uint32_t gu_phase = 0;
     bool gu_pending = false;  // a gate/up load of this warp is in flight
@@ -976,7 +993,7 @@ template <int MODE, int EPI, int CG = 1>
 static int launch(const Maps& m, const MxParams& p_in, long long tiles_bound, cudaStream_t st) {
   MxParams p = p_in;
   p.l2_elems = kL2BandBytes;  // one-byte elements
-  using L = Cfg<EPI != EPI_STORE, CG>;
+  using L = Cfg<EPI, CG>;
   auto kern = grouped_gemm_mxf8_kernel<MODE, EPI, CG>;
   static bool attr_set = false;
   static int max_units = 0;  // co-resident CTAs (CG = 1) or CTA pairs (CG = 2)
