@@ -150,6 +150,13 @@ def test_layer_checks_operand_shapes_and_dtypes(libmoe):
     # right shapes and dtypes, but host memory: refused at the pointer
     with pytest.raises(B.MoeError, match="cpu tensor"):
         L.forward(lg, x, w1, w2)
+    # the graph capture checks every buffer the same way before any CUDA call
+    dx, dl = torch.zeros(T, H, dtype=bf), torch.zeros(T, E)
+    dw1, dw2 = torch.zeros(E, H, 2 * F, dtype=bf), torch.zeros(E, F, H, dtype=bf)
+    with pytest.raises(B.MoeError, match="dlogits: expected"):
+        L.capture(lg, x, w1, w2, x, x, dx, dw1, dw2, dl.to(bf))
+    with pytest.raises(B.MoeError, match="dw1: expected"):
+        L.capture(lg, x, w1, w2, x, x, dx, dw2, dw2, dl)
 
 
 @pytest.fixture
